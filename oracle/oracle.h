@@ -1,0 +1,61 @@
+/*
+ * oracle.h -- plain CPU oracle for the block-scaled FP8 linear-layer GEMMs.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path includes, links or
+ * calls this file: only tests/, __graft_entry__.smoke() and bench.py's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * Everything is computed in double precision (fp64) with plain loops, in the
+ * order the method states it.  See oracle.c for the passage each function
+ * follows.
+ */
+#ifndef FP8LL_ORACLE_H
+#define FP8LL_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* fp8 formats named on "FP8 GEMM for the fprop should use fast accumulation"
+ * (e4m3 for fprop, e5m2 on the gradient side).  Bit layouts: OCP FP8. */
+enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1 };
+
+/* codec */
+void    oracle_fp8_decode_table(int fmt, double out[256]);
+double  oracle_fp8_max(int fmt);
+uint8_t oracle_fp8_encode(int fmt, float x);
+void    oracle_fp8_encode_array(int fmt, const float* x, int64_t n, uint8_t* q);
+
+/* bf16 helpers (bit patterns stored as uint16) */
+float    oracle_bf16_to_f32(uint16_t h);
+uint16_t oracle_f64_to_bf16(double v); /* round to nearest even, via exact comparison */
+
+/* per-128-block quantization (the page's per-token cast) */
+void oracle_quantize(int fmt, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                     int transpose, uint8_t* q, float* scale, int64_t sld);
+
+/* block-scaled GEMM: acc[i][j] = sum_kb sa*sb * sum_{k in kb} dec(qa)*dec(qb) */
+void oracle_gemm(int64_t K, int64_t k0,
+                 const uint8_t* qa, int64_t lda, const float* sa, int64_t sa_ld, int fmt_a,
+                 const uint8_t* qb, int64_t ldb, const float* sb, int64_t sb_ld, int fmt_b,
+                 const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                 double* acc, double* S);
+
+/* epilogue math */
+double oracle_gelu(double z);
+double oracle_dgelu(double z);
+void   oracle_gelu_array(const double* z, double* y, int64_t n);
+void   oracle_dgelu_array(const double* z, double* y, int64_t n);
+
+/* column sums over all rows of a dense [M][N] double matrix: bgrad[j] = sum_i dz[i][j] */
+void oracle_colsum(const double* dz, int64_t M, int64_t N, double* out);
+
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
