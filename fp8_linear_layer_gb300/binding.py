@@ -1,0 +1,217 @@
+"""ctypes binding of libfp8ll.so (include/fp8ll.h): argument marshalling only.
+
+Every computation happens in the CUDA library.  This module turns torch CUDA
+tensors into device pointers, picks torch's current stream, allocates outputs
+with torch when the caller does not pass them, and raises ``Fp8Error`` on a
+non-zero status.  There is no fallback: if the library is missing or the
+device is not supported, calls raise.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfp8ll.so")
+
+E4M3, E5M2 = 0, 1
+EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_DGELU, EPI_DGELU_BGRAD = 0, 1, 2, 3, 4
+ACC_FULL, ACC_FAST = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+
+# every symbol include/fp8ll.h declares
+EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
+           "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
+           "fp8_status_string", "fp8_debug_starve_next_gemm")
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, status_string(code), code))
+
+
+class OperandStruct(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("ld_q", ctypes.c_int64),
+                ("scale_ld", ctypes.c_int64), ("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfp8ll.so is not built (run __graft_entry__.build() or "
+                               "python fp8_linear_layer_gb300/build.py)")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        op = ctypes.POINTER(OperandStruct)
+        L.fp8_scale_ld.argtypes = [i64]
+        L.fp8_scale_ld.restype = i64
+        L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, i64, vp]
+        L.fp8_cast_f32.argtypes = [vp, i64, i32, vp, vp]
+        L.fp8_gemm_fprop.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp]
+        L.fp8_workspace_size.argtypes = [i64, i64]
+        L.fp8_workspace_size.restype = sz
+        L.fp8_gemm_dgrad.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp, sz, vp]
+        L.fp8_gemm_wgrad.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp]
+        L.fp8_grouped_wgrad.argtypes = [i32, i64, i64, ctypes.POINTER(ctypes.c_int64), op, op, vp, i32, i32, vp]
+        L.fp8_get_device_status.argtypes = [vp]
+        L.fp8_status_string.argtypes = [i32]
+        L.fp8_status_string.restype = ctypes.c_char_p
+        L.fp8_debug_starve_next_gemm.argtypes = [i32]
+        for name in ("fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_wgrad",
+                     "fp8_grouped_wgrad", "fp8_get_device_status", "fp8_debug_starve_next_gemm"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().fp8_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise Fp8Error(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def scale_ld(rows: int) -> int:
+    return int(lib().fp8_scale_ld(int(rows)))
+
+
+@dataclass
+class Fp8Tensor:
+    """fp8 codes [rows][ld_q] (uint8) with block scales [K/128][scale_ld] (fp32)."""
+    q: torch.Tensor
+    scale: torch.Tensor
+    fmt: int
+
+    @property
+    def rows(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.q.shape[1]
+
+    def operand(self) -> OperandStruct:
+        return OperandStruct(self.q.data_ptr(), self.scale.data_ptr(), self.q.stride(0),
+                             self.scale.stride(0), int(self.fmt), 0)
+
+
+def empty_fp8(rows: int, k: int, fmt: int, device="cuda") -> Fp8Tensor:
+    q = torch.empty((rows, k), dtype=torch.uint8, device=device)
+    s = torch.empty((k // 128, scale_ld(rows)), dtype=torch.float32, device=device)
+    return Fp8Tensor(q, s, fmt)
+
+
+def quantize(x: torch.Tensor, fmt: int, transpose: bool = False, out: Optional[Fp8Tensor] = None) -> Fp8Tensor:
+    """bf16 [rows][cols] -> Fp8Tensor.  transpose=False: blocks along rows, codes
+    [rows][cols]; transpose=True: blocks down columns, codes [cols][rows]."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if out is None:
+        out = empty_fp8(cols, rows, fmt, x.device) if transpose else empty_fp8(rows, cols, fmt, x.device)
+    _check(lib().fp8_quantize(_ptr(x), rows, cols, x.stride(0), int(fmt), int(bool(transpose)), _ptr(out.q),
+                              _ptr(out.scale), out.scale.stride(0), _stream()), "fp8_quantize")
+    return out
+
+
+def cast_f32(x: torch.Tensor, fmt: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    assert x.dtype == torch.float32 and x.is_contiguous()
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_cast_f32(_ptr(x), x.numel(), int(fmt), _ptr(out), _stream()), "fp8_cast_f32")
+    return out
+
+
+def gemm_fprop(A: Fp8Tensor, B: Fp8Tensor, bias: Optional[torch.Tensor] = None, epi: int = EPI_BIAS_GELU,
+               acc: int = ACC_FULL, out: Optional[torch.Tensor] = None, aux: Optional[torch.Tensor] = None,
+               want_aux: bool = True, K: Optional[int] = None):
+    """Y (bf16 [M][N]) = epilogue(A B^T); returns (Y, Z-or-None)."""
+    M, N = A.rows, B.rows
+    K = A.k if K is None else K
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if aux is None and want_aux and epi == EPI_BIAS_GELU:
+        aux = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_gemm_fprop(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(bias), int(epi), int(acc),
+                                _ptr(out), _ptr(aux), _stream()), "fp8_gemm_fprop")
+    return out, aux
+
+
+def workspace_size(M: int, N: int) -> int:
+    return int(lib().fp8_workspace_size(int(M), int(N)))
+
+
+def gemm_dgrad(A: Fp8Tensor, B: Fp8Tensor, aux: torch.Tensor, epi: int = EPI_DGELU_BGRAD, acc: int = ACC_FULL,
+               out: Optional[torch.Tensor] = None, bgrad: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, K: Optional[int] = None):
+    """dZ (bf16 [M][N]) = (A B^T) * gelu'(aux); with DGELU_BGRAD also bgrad [N].
+    Returns (dZ, bgrad-or-None)."""
+    M, N = A.rows, B.rows
+    K = A.k if K is None else K
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = 0
+    if epi == EPI_DGELU_BGRAD:
+        if bgrad is None:
+            bgrad = torch.empty((N,), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty((workspace_size(M, N) // 4,), dtype=torch.float32, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_gemm_dgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(aux), int(epi), int(acc),
+                                _ptr(out), _ptr(bgrad), _ptr(workspace), ws_bytes, _stream()), "fp8_gemm_dgrad")
+    return out, bgrad
+
+
+def gemm_wgrad(A: Fp8Tensor, B: Fp8Tensor, out: torch.Tensor, accumulate: bool = True, acc: int = ACC_FULL,
+               K: Optional[int] = None) -> torch.Tensor:
+    """fp32 out [M][N] (+)= A B^T (the weight-gradient accumulate)."""
+    M, N = A.rows, B.rows
+    K = A.k if K is None else K
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (M, N)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_gemm_wgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(out), int(bool(accumulate)),
+                                int(acc), _stream()), "fp8_gemm_wgrad")
+    return out
+
+
+def grouped_wgrad(A: Fp8Tensor, B: Fp8Tensor, k_sizes: Sequence[int], out: torch.Tensor, accumulate: bool = True,
+                  acc: int = ACC_FULL) -> torch.Tensor:
+    """fp32 out [G][M][N]: out_g (+)= A[:, group g] B[:, group g]^T, groups contiguous along K."""
+    G = len(k_sizes)
+    M, N = A.rows, B.rows
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (G, M, N)
+    ks = (ctypes.c_int64 * G)(*[int(k) for k in k_sizes])
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_grouped_wgrad(G, M, N, ks, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                   int(bool(accumulate)), int(acc), _stream()), "fp8_grouped_wgrad")
+    return out
+
+
+def device_status() -> int:
+    """Synchronizes the current stream; returns and clears the device status word."""
+    return int(lib().fp8_get_device_status(_stream()))
+
+
+def debug_starve_next_gemm(budget_ms: int):
+    _check(lib().fp8_debug_starve_next_gemm(int(budget_ms)), "fp8_debug_starve_next_gemm")

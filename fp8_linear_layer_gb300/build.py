@@ -1,0 +1,74 @@
+"""Build the CUDA library ``libfp8ll.so`` in-tree for sm_103a.
+
+Each translation unit under ``csrc/`` is compiled by nvcc in parallel
+(``-gencode arch=compute_103a,code=sm_103a``, no fast-math: the quantize
+kernel relies on IEEE division and no flush-to-zero), then linked into one
+shared library against the shared CUDA runtime.
+"""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(HERE, "libfp8ll.so")
+SOURCES = ["api.cu", "quantize.cu", "gemm_fprop.cu", "gemm_dgrad.cu", "gemm_wgrad.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc():
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def _cuda_lib_dir():
+    return os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
+
+
+def _deps():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(INCLUDE, "fp8ll.h"))
+    files.append(os.path.abspath(__file__))
+    return files
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile libfp8ll.so if missing or older than any source."""
+    if not force and os.path.exists(LIB):
+        if os.path.getmtime(LIB) >= max(os.path.getmtime(f) for f in _deps()):
+            return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
+                    "--expt-relaxed-constexpr"] + list(extra_flags)
+    if verbose:
+        flags += ["-Xptxas", "-v"]
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        cmd = [_nvcc()] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stdout + r.stderr))
+        return obj, r.stdout + r.stderr
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    if verbose:
+        for _, log in results:
+            sys.stderr.write(log)
+    tmp = LIB + ".tmp%d" % os.getpid()
+    cmd = [_nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + [o for o, _ in results] + \
+        ["-Xlinker", "-rpath", "-Xlinker", _cuda_lib_dir()]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stdout + r.stderr))
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,371 @@
+// api.cu -- the C ABI (include/fp8ll.h): host-side validation, TMA descriptor
+// encoding, device checks and kernel launches.  No allocation, no implicit
+// synchronization (fp8_get_device_status excepted).
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fp8ll.h"
+#include "internal.h"
+
+namespace fp8ll {
+
+// Device status word: kernels record the first pipeline time-out here.
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr uint64_t kDefaultBudgetNs = 2000000000ull;  // 2 s per pipeline wait
+
+struct DeviceInfo {
+    bool checked = false;
+    bool supported = false;
+    int num_sms = 0;
+    int* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[64];
+std::atomic<int> g_starve_ms{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Current device; checks it is sm_103 and caches SM count and status address.
+int current_device(DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8LL_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8LL_ERR_LAUNCH;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FP8LL_ERR_LAUNCH;
+            d.status = static_cast<int*>(p);
+        }
+        d.checked = true;
+    }
+    if (!d.supported) return FP8LL_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return FP8LL_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_fmt(int f) { return f == FP8LL_E4M3 || f == FP8LL_E5M2; }
+
+// Checks one GEMM operand with `rows` rows and a K extent of `kext` columns.
+bool valid_operand(const fp8ll_operand_t* op, int64_t rows, int64_t kext) {
+    if (!op || !op->q || !op->scale) return false;
+    if (!aligned16(op->q) || !aligned16(op->scale)) return false;
+    if (!valid_fmt(op->fmt)) return false;
+    if (op->ld_q < kext || op->ld_q % 16 != 0 || op->ld_q >= (1LL << 39)) return false;
+    if (op->scale_ld < rows || op->scale_ld % 4 != 0 || op->scale_ld >= (1LL << 36)) return false;
+    if (rows < 1 || rows > (1LL << 31) - 1) return false;
+    return true;
+}
+
+// TMA descriptors for one operand: codes [rows][kext] (row stride ld_q) in
+// 128 x box_rows byte boxes with 128-byte swizzle; scales [kext/128][scale_ld]
+// in box_rows x 1 boxes.  Out-of-range rows read as zero.
+bool encode_operand(const fp8ll_operand_t* op, int64_t rows, int64_t kext, uint32_t box_rows, CUtensorMap* qmap,
+                    CUtensorMap* smap) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kext), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(op->ld_q)};
+        const cuuint32_t box[2] = {128, box_rows};
+        if (enc(qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(op->q), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(kext / 128)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(op->scale_ld) * 4};
+        const cuuint32_t box[2] = {box_rows, 1};
+        if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(op->scale), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+void init_params(GemmParams& p, int64_t M, int64_t N, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                 const DeviceInfo* dev) {
+    std::memset(&p, 0, sizeof(p));
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.num_m_tiles = static_cast<int32_t>((M + 127) / 128);
+    p.num_n_tiles = static_cast<int32_t>((N + 255) / 256);
+    p.tiles_per_group = p.num_m_tiles * p.num_n_tiles;
+    p.idesc = (1u << 4) | (static_cast<uint32_t>(A->fmt) << 7) | (static_cast<uint32_t>(B->fmt) << 10) |
+              ((256u >> 3) << 17) | ((128u >> 4) << 24);
+    p.status = dev->status;
+    const int starve = g_starve_ms.exchange(0);
+    if (starve > 0) {
+        p.debug_starve = 1;
+        p.budget_ns = static_cast<uint64_t>(starve) * 1000000ull;
+    } else {
+        p.budget_ns = kDefaultBudgetNs;
+    }
+}
+
+int grid_for(const GemmParams& p, const DeviceInfo* dev) {
+    return p.total_tiles < dev->num_sms ? p.total_tiles : dev->num_sms;
+}
+
+bool valid_mn(int64_t M, int64_t N) {
+    if (M < 1 || N < 1 || M > (1LL << 31) - 1 || N > (1LL << 31) - 1) return false;
+    const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+    return tiles < (1LL << 30) && M * N < (1LL << 46);
+}
+
+}  // namespace
+}  // namespace fp8ll
+
+using namespace fp8ll;
+
+extern "C" {
+
+int64_t fp8_scale_ld(int64_t rows) { return rows <= 0 ? 0 : (rows + 3) / 4 * 4; }
+
+int fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                 float* scale, int64_t scale_ld, fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !valid_fmt(fmt) || (transpose != 0 && transpose != 1)) return FP8LL_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8LL_OK;
+    if (!x_bf16 || !q || !scale || !aligned16(x_bf16) || !aligned16(q) || !aligned16(scale))
+        return FP8LL_ERR_INVALID_ARG;
+    if (ldx < cols || ldx % 8 != 0 || scale_ld % 4 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (rows > (1LL << 31) - 1 || cols > (1LL << 31) - 1) return FP8LL_ERR_INVALID_ARG;
+    if (!transpose) {
+        if (cols % 128 != 0 || scale_ld < rows) return FP8LL_ERR_INVALID_ARG;
+    } else {
+        if (rows % 128 != 0 || cols % 8 != 0 || scale_ld < cols) return FP8LL_ERR_INVALID_ARG;
+        if (rows / 128 > 65535) return FP8LL_ERR_INVALID_ARG;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_quantize(x_bf16, rows, cols, ldx, fmt, transpose, q, scale, scale_ld,
+                           reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, fp8ll_stream_t stream) {
+    if (n < 0 || !valid_fmt(fmt)) return FP8LL_ERR_INVALID_ARG;
+    if (n == 0) return FP8LL_OK;
+    if (!x || !q || !aligned16(x) || !aligned16(q)) return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_cast_f32(x, n, fmt, q, reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                   const void* bias_bf16, int epi, int acc_mode, void* out_bf16, void* aux_bf16,
+                   fp8ll_stream_t stream) {
+    if (!valid_mn(M, N) || K < 128 || K % 128 != 0 || K >= (1LL << 36)) return FP8LL_ERR_INVALID_ARG;
+    if (epi != FP8LL_EPI_NONE && epi != FP8LL_EPI_BIAS && epi != FP8LL_EPI_BIAS_GELU) return FP8LL_ERR_INVALID_ARG;
+    if (acc_mode != FP8LL_ACC_FULL && acc_mode != FP8LL_ACC_FAST) return FP8LL_ERR_INVALID_ARG;
+    if (!valid_operand(A, M, K) || !valid_operand(B, N, K)) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi != FP8LL_EPI_NONE && (!bias_bf16 || !aligned16(bias_bf16))) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    TensorMaps maps;
+    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, 256, &maps.b, &maps.sb))
+        return FP8LL_ERR_LAUNCH;
+    GemmParams p;
+    init_params(p, M, N, A, B, dev);
+    p.num_groups = 1;
+    p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
+    p.total_tiles = p.tiles_per_group;
+    p.out = out_bf16;
+    p.aux = (epi == FP8LL_EPI_BIAS_GELU) ? aux_bf16 : nullptr;
+    p.bias = bias_bf16;
+    return launch_gemm_fprop(maps, p, epi, acc_mode, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+size_t fp8_workspace_size(int64_t M, int64_t N) {
+    if (M < 1 || N < 1) return 0;
+    return static_cast<size_t>((M + 127) / 128) * 4 * static_cast<size_t>(N) * sizeof(float);
+}
+
+int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                   const void* aux_bf16, int epi, int acc_mode, void* out_bf16, float* bgrad, void* workspace,
+                   size_t workspace_bytes, fp8ll_stream_t stream) {
+    if (!valid_mn(M, N) || K < 128 || K % 128 != 0 || K >= (1LL << 36)) return FP8LL_ERR_INVALID_ARG;
+    if (epi != FP8LL_EPI_DGELU && epi != FP8LL_EPI_DGELU_BGRAD) return FP8LL_ERR_INVALID_ARG;
+    if (acc_mode != FP8LL_ACC_FULL && acc_mode != FP8LL_ACC_FAST) return FP8LL_ERR_INVALID_ARG;
+    if (!valid_operand(A, M, K) || !valid_operand(B, N, K)) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16) || !aux_bf16 || !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_DGELU_BGRAD) {
+        if (!bgrad || !aligned16(bgrad)) return FP8LL_ERR_INVALID_ARG;
+        if (!workspace || !aligned16(workspace) || workspace_bytes < fp8_workspace_size(M, N))
+            return FP8LL_ERR_WORKSPACE;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    TensorMaps maps;
+    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, 256, &maps.b, &maps.sb))
+        return FP8LL_ERR_LAUNCH;
+    GemmParams p;
+    init_params(p, M, N, A, B, dev);
+    p.num_groups = 1;
+    p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
+    p.total_tiles = p.tiles_per_group;
+    p.out = out_bf16;
+    p.aux = const_cast<void*>(aux_bf16);
+    p.workspace = static_cast<float*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_gemm_dgrad(maps, p, epi, acc_mode, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
+    if (epi == FP8LL_EPI_DGELU_BGRAD) {
+        if (launch_bgrad_finalize(static_cast<const float*>(workspace), static_cast<int64_t>(p.num_m_tiles) * 4, N,
+                                  bgrad, s, dev->num_sms) != 0)
+            return FP8LL_ERR_LAUNCH;
+    }
+    return FP8LL_OK;
+}
+
+int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const fp8ll_operand_t* A,
+                      const fp8ll_operand_t* B, float* out, int accumulate, int acc_mode, fp8ll_stream_t stream) {
+    if (G < 1 || G > kMaxGroups || !k_sizes) return FP8LL_ERR_INVALID_ARG;
+    if (!valid_mn(M, N) || (accumulate != 0 && accumulate != 1)) return FP8LL_ERR_INVALID_ARG;
+    if (acc_mode != FP8LL_ACC_FULL && acc_mode != FP8LL_ACC_FAST) return FP8LL_ERR_INVALID_ARG;
+    if (!out || !aligned16(out)) return FP8LL_ERR_INVALID_ARG;
+    int64_t total_k = 0;
+    for (int g = 0; g < G; ++g) {
+        if (k_sizes[g] < 0 || k_sizes[g] % 128 != 0) return FP8LL_ERR_INVALID_ARG;
+        total_k += k_sizes[g];
+        if (total_k >= (1LL << 36)) return FP8LL_ERR_INVALID_ARG;
+    }
+    if (static_cast<int64_t>(G) * M * N >= (1LL << 46)) return FP8LL_ERR_INVALID_ARG;
+    if (total_k > 0 && (!valid_operand(A, M, total_k) || !valid_operand(B, N, total_k)))
+        return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t slab = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+    GemmParams p;
+    int ng = 0;
+    if (total_k > 0) init_params(p, M, N, A, B, dev);
+    // groups with work, longest first (ties keep their order) for load balance
+    int order[kMaxGroups];
+    for (int g = 0; g < G; ++g) order[g] = g;
+    for (int i = 1; i < G; ++i) {
+        const int v = order[i];
+        int j = i - 1;
+        while (j >= 0 && k_sizes[order[j]] < k_sizes[v]) {
+            order[j + 1] = order[j];
+            --j;
+        }
+        order[j + 1] = v;
+    }
+    int64_t offs[kMaxGroups];
+    int64_t acc_off = 0;
+    for (int g = 0; g < G; ++g) {
+        offs[g] = acc_off;
+        acc_off += k_sizes[g];
+    }
+    for (int i = 0; i < G; ++i) {
+        const int g = order[i];
+        if (k_sizes[g] == 0) {
+            // an empty group contributes nothing: keep out_g, or zero it for out =
+            if (!accumulate && cudaMemsetAsync(out + static_cast<size_t>(g) * M * N, 0, slab, s) != cudaSuccess)
+                return FP8LL_ERR_LAUNCH;
+            continue;
+        }
+        p.groups[ng++] = GroupEntry{static_cast<int32_t>(offs[g] / 128), static_cast<int32_t>(k_sizes[g] / 128), g, 0};
+    }
+    if (ng == 0) return FP8LL_OK;
+    TensorMaps maps;
+    if (!encode_operand(A, M, total_k, 128, &maps.a, &maps.sa) ||
+        !encode_operand(B, N, total_k, 256, &maps.b, &maps.sb))
+        return FP8LL_ERR_LAUNCH;
+    p.num_groups = ng;
+    p.total_tiles = ng * p.tiles_per_group;
+    p.out = out;
+    p.accumulate = accumulate;
+    return launch_gemm_wgrad(maps, p, acc_mode, s, grid_for(p, dev)) == 0 ? FP8LL_OK : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                   float* out, int accumulate, int acc_mode, fp8ll_stream_t stream) {
+    if (K < 0) return FP8LL_ERR_INVALID_ARG;
+    const int64_t ks[1] = {K};
+    return fp8_grouped_wgrad(1, M, N, ks, A, B, out, accumulate, acc_mode, stream);
+}
+
+int fp8_get_device_status(fp8ll_stream_t stream) {
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8LL_ERR_LAUNCH;
+    int v = 0;
+    if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8LL_ERR_LAUNCH;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8LL_ERR_LAUNCH;
+    }
+    return v;
+}
+
+const char* fp8_status_string(int code) {
+    switch (code) {
+        case FP8LL_OK: return "ok";
+        case FP8LL_ERR_INVALID_ARG: return "invalid argument";
+        case FP8LL_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+        case FP8LL_ERR_LAUNCH: return "CUDA launch or driver error";
+        case FP8LL_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+        case FP8LL_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int fp8_debug_starve_next_gemm(int budget_ms) {
+    if (budget_ms < 1 || budget_ms > 10000) return FP8LL_ERR_INVALID_ARG;
+    g_starve_ms.store(budget_ms);
+    return FP8LL_OK;
+}
+
+}  // extern "C"

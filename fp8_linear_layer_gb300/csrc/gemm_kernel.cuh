@@ -1,0 +1,494 @@
+// gemm_kernel.cuh -- persistent block-scaled FP8 GEMM for sm_103a (tcgen05 + TMA + TMEM).
+//
+// Computes, for every output tile, C[i][j] = sum_kb sA[kb][i] sB[kb][j] P_kb[i][j]
+// with P_kb[i][j] = sum_{k in block kb} qA[i][k] qB[j][k] (raw fp8 products,
+// fp32 in TMEM), i.e. the 1x128 block-scaled "nt" GEMM of "Weight gradient
+// kernels for dense and MoE models", then applies one of the fused epilogues
+// of "Replaced cublasLt calls with rocblas gemm + 6 manually crafted
+// epilogues" (bias, tanh-GELU, GELU derivative, bias-gradient column sums) or
+// the fp32 weight-gradient read-modify-write (out += C).
+//
+// CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
+// rasterized tile list:
+//   warp 0      TMA producer: operand tiles (128 x 128 B and 256 x 128 B,
+//               128-byte swizzle) into a 4-stage ring, block scales into an
+//               8-stage ring.
+//   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
+//               (M=128, N=256, K=32, kind::f8f6f4) into one of two TMEM
+//               accumulators (2 x 256 fp32 columns = all 512 columns).
+//   warps 2-3   idle (they complete the first warpgroup).
+//   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4)..+31
+//               (its rows) and one half of the columns; per K block each
+//               thread adds sA*sB*P into a 128-wide fp32 register accumulator
+//               ("promotion"), releasing the TMEM buffer to the MMA warp so
+//               the next block's MMA overlaps this block's promotion.
+// Registers: launched at kLaunchRegs per thread (the most 384 threads can
+// have), the first warpgroup gives registers back (setmaxnreg.dec to
+// kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
+// kRegsEpi); 128 * kRegsCtrl + 256 * kRegsEpi <= 384 * kLaunchRegs.  The host
+// refuses to launch if the compiled kernel's register count differs from
+// kLaunchRegs, so the split can never ask for more than the pool.
+// All pipeline waits are bounded (see ptx.cuh); a wait that runs out records
+// a time-out in the status word and every role winds down without touching
+// the outputs further.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8ll {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 128;  // K bytes per stage == one scale block
+constexpr int kStages = 4;
+constexpr int kSStages = 8;
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kThreads = 128 + 32 * kEpiWarps;
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtrl = 48;
+constexpr int kRegsEpi = 224;
+static_assert(128 * kRegsCtrl + 256 * kRegsEpi <= kThreads * kLaunchRegs, "register split exceeds the pool");
+constexpr int kHalfN = kBN / 2;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kRasterM = 16;
+
+struct __align__(1024) SmemLayout {
+    uint8_t a[kStages][kBM * kBK];
+    uint8_t b[kStages][kBN * kBK];
+    float sa[kSStages][kBM];
+    float sb[kSStages][kBN];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t sfull[kSStages];
+    uint64_t sempty[kSStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = sizeof(SmemLayout) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+template <int N>
+__device__ __forceinline__ void ring_advance(int& idx, uint32_t& phase) {
+    if (++idx == N) {
+        idx = 0;
+        phase ^= 1u;
+    }
+}
+
+// tile index -> (group, m tile, n tile); within a group, bands of kRasterM
+// row-tiles are walked column by column so that concurrently running CTAs
+// share operand rows in L2.
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, int& mt, int& nt) {
+    g = t / p.tiles_per_group;
+    const int local = t - g * p.tiles_per_group;
+    const int band_tiles = kRasterM * p.num_n_tiles;
+    const int band = local / band_tiles;
+    const int first_m = band * kRasterM;
+    const int rem_m = p.num_m_tiles - first_m;
+    const int bm = rem_m < kRasterM ? rem_m : kRasterM;
+    const int r = local - band * band_tiles;
+    mt = first_m + r % bm;
+    nt = r / bm;
+}
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v) != 0; }
+
+// ------------------------------------------------------------------ stores
+
+// wgrad: out (+)= acc, fp32
+__device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, int r, int cbase,
+                                            float (&acc)[kHalfN]) {
+    if (r >= p.M) return;
+    float* orow = static_cast<float*>(p.out) + (static_cast<int64_t>(out_index) * p.M + r) * p.N + cbase;
+    if ((p.N & 3) == 0 && cbase + kHalfN <= p.N) {
+        if (p.accumulate) {
+#pragma unroll
+            for (int j = 0; j < kHalfN; j += 4) {
+                float4 o = *reinterpret_cast<const float4*>(orow + j);
+                o.x += acc[j];
+                o.y += acc[j + 1];
+                o.z += acc[j + 2];
+                o.w += acc[j + 3];
+                *reinterpret_cast<float4*>(orow + j) = o;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kHalfN; j += 4)
+                *reinterpret_cast<float4*>(orow + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kHalfN; ++j) {
+            if (cbase + j < p.N) orow[j] = (p.accumulate ? orow[j] : 0.0f) + acc[j];
+        }
+    }
+}
+
+// fprop: Z = acc + bias[j]; Y = gelu(Z) or Z; bf16 out (+ bf16 aux Z)
+template <int EPI>
+__device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbase, float (&acc)[kHalfN]) {
+    if (r >= p.M) return;
+    const int64_t off = static_cast<int64_t>(r) * p.N + cbase;
+    uint16_t* out = static_cast<uint16_t*>(p.out) + off;
+    uint16_t* aux = (EPI == kEpiBiasGelu && p.aux) ? static_cast<uint16_t*>(p.aux) + off : nullptr;
+    const uint16_t* bias = static_cast<const uint16_t*>(p.bias) + cbase;
+    if ((p.N & 7) == 0 && cbase + kHalfN <= p.N) {
+#pragma unroll
+        for (int j = 0; j < kHalfN; j += 8) {
+            float z[8];
+            if (EPI == kEpiNone) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) z[i] = acc[j + i];
+            } else {
+                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + j));
+                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    z[2 * i] = acc[j + 2 * i] + bf16_lo(bw[i]);
+                    z[2 * i + 1] = acc[j + 2 * i + 1] + bf16_hi(bw[i]);
+                }
+            }
+            uint32_t yw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (EPI == kEpiBiasGelu)
+                    yw[i] = pack_bf16x2(gelu_tanh(z[2 * i]), gelu_tanh(z[2 * i + 1]));
+                else
+                    yw[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+            }
+            *reinterpret_cast<uint4*>(out + j) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+            if (aux) {
+                *reinterpret_cast<uint4*>(aux + j) =
+                    make_uint4(pack_bf16x2(z[0], z[1]), pack_bf16x2(z[2], z[3]), pack_bf16x2(z[4], z[5]),
+                               pack_bf16x2(z[6], z[7]));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kHalfN; ++j) {
+            if (cbase + j < p.N) {
+                float z = acc[j];
+                if (EPI != kEpiNone) z += __uint_as_float(static_cast<uint32_t>(bias[j]) << 16);
+                const float y = (EPI == kEpiBiasGelu) ? gelu_tanh(z) : z;
+                out[j] = static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu);
+                if (aux) aux[j] = static_cast<uint16_t>(pack_bf16x2(z, 0.0f) & 0xFFFFu);
+            }
+        }
+    }
+}
+
+// dgrad: dZ = acc * gelu'(Z); bf16 out.  acc is overwritten with the fp32 dZ
+// (zero outside the matrix) for the bias-gradient sums.
+__device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbase, float (&acc)[kHalfN]) {
+    if (r >= p.M) {
+#pragma unroll
+        for (int j = 0; j < kHalfN; ++j) acc[j] = 0.0f;
+        return;
+    }
+    const int64_t off = static_cast<int64_t>(r) * p.N + cbase;
+    uint16_t* out = static_cast<uint16_t*>(p.out) + off;
+    const uint16_t* zp = static_cast<const uint16_t*>(p.aux) + off;
+    if ((p.N & 7) == 0 && cbase + kHalfN <= p.N) {
+#pragma unroll
+        for (int j = 0; j < kHalfN; j += 8) {
+            const uint4 zv = *reinterpret_cast<const uint4*>(zp + j);
+            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float d0 = acc[j + 2 * i] * dgelu_tanh(bf16_lo(zw[i]));
+                const float d1 = acc[j + 2 * i + 1] * dgelu_tanh(bf16_hi(zw[i]));
+                acc[j + 2 * i] = d0;
+                acc[j + 2 * i + 1] = d1;
+                ow[i] = pack_bf16x2(d0, d1);
+            }
+            *reinterpret_cast<uint4*>(out + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kHalfN; ++j) {
+            if (cbase + j < p.N) {
+                const float z = __uint_as_float(static_cast<uint32_t>(zp[j]) << 16);
+                const float d = acc[j] * dgelu_tanh(z);
+                acc[j] = d;
+                out[j] = static_cast<uint16_t>(pack_bf16x2(d, 0.0f) & 0xFFFFu);
+            } else {
+                acc[j] = 0.0f;
+            }
+        }
+    }
+}
+
+// Column sums of 32 consecutive columns over the 32 rows held by a warp:
+// a butterfly that halves the column set at each step.  Afterwards lane l
+// holds the sum for column l.  The summation order is fixed, so results are
+// deterministic.
+__device__ __forceinline__ float warp_column_sum32(float (&v)[kHalfN], int c0, int lane) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[c0 + i] : v[c0 + i + off];
+            const float keep = upper ? v[c0 + i + off] : v[c0 + i];
+            v[c0 + i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[c0];
+}
+
+// -------------------------------------------------------------------- kernel
+
+template <int EPI, bool FAST>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    SmemLayout& sm = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                    ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t budget = p.budget_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&sm.full[s]), 1);
+            mbar_init(smem_addr(&sm.empty[s]), 1);
+        }
+        for (int s = 0; s < kSStages; ++s) {
+            mbar_init(smem_addr(&sm.sfull[s]), 1);
+            mbar_init(smem_addr(&sm.sempty[s]), kEpiWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&sm.acc_full[b]), 1);
+            mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
+        }
+        mbar_init(smem_addr(&sm.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+
+    if (warp < kFirstEpiWarp) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.a);
+            tma_prefetch_desc(&maps.b);
+            tma_prefetch_desc(&maps.sa);
+            tma_prefetch_desc(&maps.sb);
+            int s = 0, ss = 0;
+            uint32_t ph = 0, sph = 0;
+            int n_issued = 0, ns_issued = 0;
+            bool ok = true;
+            if (!p.debug_starve) {
+                for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                    int g, mt, nt;
+                    decode_tile(p, t, g, mt, nt);
+                    const GroupEntry ge = p.groups[g];
+                    const int m0 = mt * kBM, n0 = nt * kBN;
+                    for (int kb = 0; kb < ge.nkb; ++kb) {
+                        const int kbg = ge.kb_start + kb;
+                        if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, budget)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = smem_addr(&sm.full[s]);
+                        mbar_arrive_expect_tx(fb, kBM * kBK + kBN * kBK);
+                        tma_load_2d(smem_addr(sm.a[s]), &maps.a, fb, kbg * kBK, m0);
+                        tma_load_2d(smem_addr(sm.b[s]), &maps.b, fb, kbg * kBK, n0);
+                        ++n_issued;
+                        ring_advance<kStages>(s, ph);
+                        if (!mbar_wait(smem_addr(&sm.sempty[ss]), sph ^ 1u, budget)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sfb = smem_addr(&sm.sfull[ss]);
+                        mbar_arrive_expect_tx(sfb, (kBM + kBN) * 4);
+                        tma_load_2d(smem_addr(sm.sa[ss]), &maps.sa, sfb, m0, kbg);
+                        tma_load_2d(smem_addr(sm.sb[ss]), &maps.sb, sfb, n0, kbg);
+                        ++ns_issued;
+                        ring_advance<kSStages>(ss, sph);
+                    }
+                }
+            }
+            if (ok) {
+                // every stage must be released by its consumer before exit
+                for (int i = 0; i < kStages; ++i) {
+                    if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, budget)) ok = false;
+                    ring_advance<kStages>(s, ph);
+                }
+                for (int i = 0; i < kSStages; ++i) {
+                    if (!mbar_wait(smem_addr(&sm.sempty[ss]), sph ^ 1u, budget)) ok = false;
+                    ring_advance<kSStages>(ss, sph);
+                }
+            }
+            if (!ok) {
+                record_status(p.status, kStatusTimeout);
+                // let the loads still in flight land before shared memory goes away
+                for (int i = 1; i <= (n_issued < kStages ? n_issued : kStages); ++i) {
+                    int si = s - i;
+                    uint32_t pi = ph;
+                    if (si < 0) {
+                        si += kStages;
+                        pi ^= 1u;
+                    }
+                    mbar_wait(smem_addr(&sm.full[si]), pi, budget);
+                }
+                for (int i = 1; i <= (ns_issued < kSStages ? ns_issued : kSStages); ++i) {
+                    int si = ss - i;
+                    uint32_t pi = sph;
+                    if (si < 0) {
+                        si += kSStages;
+                        pi ^= 1u;
+                    }
+                    mbar_wait(smem_addr(&sm.sfull[si]), pi, budget);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        int s = 0, ab = 0;
+        uint32_t ph = 0, aph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            int g, mt, nt;
+            decode_tile(p, t, g, mt, nt);
+            const int nkb = p.groups[g].nkb;
+            for (int kb = 0; kb < nkb; ++kb) {
+                ok = warp_all(mbar_wait(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget));
+                if (ok) ok = warp_all(mbar_wait(smem_addr(&sm.full[s]), ph, budget));
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(ab * kBN);
+                    const uint64_t adesc = smem_desc_k_sw128(smem_addr(sm.a[s]));
+                    const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sm.b[s]));
+#pragma unroll
+                    for (int k = 0; k < kBK / 32; ++k)
+                        mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, p.idesc, k > 0 ? 1u : 0u);
+                    mma_commit(smem_addr(&sm.empty[s]));
+                    mma_commit(smem_addr(&sm.acc_full[ab]));
+                }
+                __syncwarp();
+                ring_advance<kStages>(s, ph);
+                ring_advance<2>(ab, aph);
+            }
+        }
+        if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
+        // all MMAs issued by this warp must complete before TMEM is released
+        if (lane == 0) mma_commit(smem_addr(&sm.drain));
+        __syncwarp();
+        mbar_wait(smem_addr(&sm.drain), 0, budget);
+        __syncwarp();
+    } else if (warp >= kFirstEpiWarp) {
+        // ------------------------------------------ promotion and epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+        const int ew = warp - kFirstEpiWarp;
+        const int q = warp & 3;        // TMEM lane quadrant of this warp
+        const int half = ew >> 2;      // which 128 columns of the tile
+        const int row = q * 32 + lane; // row within the tile
+        int ab = 0, ss = 0;
+        uint32_t aph = 0, sph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            int g, mt, nt;
+            decode_tile(p, t, g, mt, nt);
+            const GroupEntry ge = p.groups[g];
+            const int m0 = mt * kBM, n0 = nt * kBN;
+            float acc[kHalfN];
+#pragma unroll
+            for (int j = 0; j < kHalfN; ++j) acc[j] = 0.0f;
+            for (int kb = 0; kb < ge.nkb; ++kb) {
+                ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
+                if (ok) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
+                if (!ok) break;
+                tc_fence_after();
+                const float sa = sm.sa[ss][row];
+                const float* sbp = &sm.sb[ss][half * kHalfN];
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(ab * kBN + half * kHalfN);
+#pragma unroll
+                for (int c = 0; c < kHalfN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 sb4 = *reinterpret_cast<const float4*>(sbp + c * 32 + j);
+                        acc[c * 32 + j + 0] = fmaf(__uint_as_float(r[j + 0]), sa * sb4.x, acc[c * 32 + j + 0]);
+                        acc[c * 32 + j + 1] = fmaf(__uint_as_float(r[j + 1]), sa * sb4.y, acc[c * 32 + j + 1]);
+                        acc[c * 32 + j + 2] = fmaf(__uint_as_float(r[j + 2]), sa * sb4.z, acc[c * 32 + j + 2]);
+                        acc[c * 32 + j + 3] = fmaf(__uint_as_float(r[j + 3]), sa * sb4.w, acc[c * 32 + j + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+                    mbar_arrive(smem_addr(&sm.sempty[ss]));
+                }
+                ring_advance<2>(ab, aph);
+                ring_advance<kSStages>(ss, sph);
+            }
+            if (!ok) break;
+            const int r = m0 + row;
+            const int cbase = n0 + half * kHalfN;
+            if (EPI == kEpiWgrad) {
+                store_wgrad(p, ge.out_index, r, cbase, acc);
+            } else if (EPI == kEpiNone || EPI == kEpiBias || EPI == kEpiBiasGelu) {
+                store_fprop<EPI>(p, r, cbase, acc);
+            } else {
+                store_dgrad(p, r, cbase, acc);
+                if (EPI == kEpiDgeluBgrad) {
+                    // partial column sums of this warp's 32 rows -> workspace band (4*mt + q)
+                    float* band = p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N;
+#pragma unroll
+                    for (int c = 0; c < kHalfN / 32; ++c) {
+                        const float v = warp_column_sum32(acc, c * 32, lane);
+                        const int col = cbase + c * 32 + lane;
+                        if (col < p.N) band[col] = v;
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int EPI, bool FAST>
+int launch_gemm_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid) {
+    auto kern = gemm_fp8_kernel<EPI, FAST>;
+    static unsigned long long configured = 0;  // one bit per device ordinal
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
+    if (!(configured & (1ull << dev))) {
+        // the register split above assumes exactly kLaunchRegs per thread at launch
+        cudaFuncAttributes attr;
+        if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess || attr.numRegs != kLaunchRegs) return -3;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
+            return -3;
+        configured |= 1ull << dev;
+    }
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace fp8ll

@@ -1,0 +1,65 @@
+// internal.h -- host-side interfaces between the C-ABI layer and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8ll {
+
+constexpr int kMaxGroups = 256;
+
+enum EpiKind : int {
+    kEpiNone = 0,
+    kEpiBias = 1,
+    kEpiBiasGelu = 2,
+    kEpiDgelu = 3,
+    kEpiDgeluBgrad = 4,
+    kEpiWgrad = 5,  // fp32 out (+)= C
+};
+
+// One schedulable group of output tiles: all tiles of a group share the same
+// K range.  Dense GEMMs have a single group.
+struct GroupEntry {
+    int32_t kb_start;  // first 128-deep K block (also the scale row index)
+    int32_t nkb;       // number of K blocks (0 allowed for zero-filling)
+    int32_t out_index; // which M x N output slab the group writes
+    int32_t pad;
+};
+
+struct GemmParams {
+    int32_t M, N;
+    int32_t num_m_tiles, num_n_tiles;
+    int32_t tiles_per_group;
+    int32_t num_groups;
+    int32_t total_tiles;
+    int32_t accumulate;   // wgrad: 1 = out +=, 0 = out =
+    int32_t debug_starve; // test hook: producer issues no loads
+    uint32_t idesc;       // tcgen05 instruction descriptor (formats, tile shape)
+    uint64_t budget_ns;   // wall-clock budget of each pipeline wait
+    void* out;            // bf16 [M][N] (fprop/dgrad) or fp32 [G][M][N] (wgrad)
+    void* aux;            // bf16 [M][N]: Z written by fprop BIAS_GELU, read by dgrad
+    const void* bias;     // bf16 [N]
+    float* workspace;     // fp32 [4 * num_m_tiles][N] bias-gradient partials (one per 32-row band)
+    int* status;          // device status word
+    GroupEntry groups[kMaxGroups];
+};
+
+struct TensorMaps {
+    CUtensorMap a, b, sa, sb;
+};
+
+int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                    float* scale, int64_t sld, cudaStream_t stream, int num_sms);
+int launch_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, cudaStream_t stream, int num_sms);
+
+// GEMM launchers, one per epilogue family (separate translation units).
+int launch_gemm_fprop(const TensorMaps& maps, const GemmParams& p, int epi, int fast, cudaStream_t stream,
+                      int grid);
+int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, int fast, cudaStream_t stream,
+                      int grid);
+int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, int fast, cudaStream_t stream, int grid);
+int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* bgrad, cudaStream_t stream,
+                          int num_sms);
+size_t gemm_smem_bytes();
+
+}  // namespace fp8ll

@@ -1,0 +1,247 @@
+// quantize.cu -- bf16 -> fp8 (e4m3 / e5m2) per-128-block cast kernels.
+//
+// "Weight gradient kernels for dense and MoE models" casts both GEMM operands
+// per token with one fp32 scale per 128 elements before the fp8 GEMM; the
+// per-block rule implemented here (and in the oracle, independently) is
+//   amax = max|x|, inv = fl32(FMAX/amax), scale = fl32(amax/FMAX),
+//   q = RNE-saturating fp8(fl32(x * inv)),
+// with inv = scale = 1 for a block whose amax is 0 or whose FMAX/amax
+// overflows fp32.  Division and multiplication are IEEE round-to-nearest
+// (__fdiv_rn / __fmul_rn, no flush-to-zero), so codes and scales are
+// bit-reproducible.
+//
+// Both kernels are HBM-bound: 2 bytes read + 1 byte + 4/128 bytes written per
+// element.
+#include <cfloat>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8ll {
+
+template <int FMT>
+struct Fp8Fmt;
+template <>
+struct Fp8Fmt<0> {
+    static constexpr float kMax = 448.0f;
+    __device__ static uint16_t cvt2(float lo, float hi) { return cvt_e4m3x2(lo, hi); }
+};
+template <>
+struct Fp8Fmt<1> {
+    static constexpr float kMax = 57344.0f;
+    __device__ static uint16_t cvt2(float lo, float hi) { return cvt_e5m2x2(lo, hi); }
+};
+
+template <int FMT>
+__device__ __forceinline__ void block_scale(float amax, float& inv, float& scale) {
+    inv = 1.0f;
+    scale = 1.0f;
+    if (amax > 0.0f) {
+        const float t = __fdiv_rn(Fp8Fmt<FMT>::kMax, amax);
+        if (t <= FLT_MAX) {
+            inv = t;
+            scale = __fdiv_rn(amax, Fp8Fmt<FMT>::kMax);
+        }
+    }
+}
+
+// 8 values -> 8 codes packed little-endian in a uint2
+template <int FMT>
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], float inv) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = __fmul_rn(f[2 * i], inv);
+        const float b = __fmul_rn(f[2 * i + 1], inv);
+        w[i] = Fp8Fmt<FMT>::cvt2(a, b);
+    }
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+// ------------------------------------------------------------------ row-wise
+// A half-warp owns one (row, 128-block) task: 16 lanes x 16 bytes of bf16.
+// Consecutive tasks are consecutive blocks of a row, so a warp reads 512
+// contiguous bytes.  Each warp keeps U task pairs in flight.
+template <int FMT, int U>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                            int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
+                                                            float* __restrict__ scale, int64_t sld) {
+    const int64_t nb = cols / 128;
+    const int64_t total = rows * nb;
+    const int lane = threadIdx.x & 31;
+    const int hl = lane & 15;
+    const int hw = lane >> 4;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+
+    for (int64_t base = warp * 2 * U; base < total; base += nwarps * 2 * U) {
+        uint4 v[U];
+        int64_t task[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            task[u] = base + 2 * u + hw;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (task[u] < total) {
+                const int64_t r = task[u] / nb;
+                const int64_t b = task[u] - r * nb;
+                v[u] = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + b * 128 + hl * 8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float f[8];
+            f[0] = bf16_lo(v[u].x); f[1] = bf16_hi(v[u].x);
+            f[2] = bf16_lo(v[u].y); f[3] = bf16_hi(v[u].y);
+            f[4] = bf16_lo(v[u].z); f[5] = bf16_hi(v[u].z);
+            f[6] = bf16_lo(v[u].w); f[7] = bf16_hi(v[u].w);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            float inv, s;
+            block_scale<FMT>(amax, inv, s);
+            const uint2 codes = encode8<FMT>(f, inv);
+            if (task[u] < total) {
+                const int64_t r = task[u] / nb;
+                const int64_t b = task[u] - r * nb;
+                *reinterpret_cast<uint2*>(q + r * cols + b * 128 + hl * 8) = codes;
+                if (hl == 0) scale[b * sld + r] = s;
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------- transposed
+// One CTA owns a 128-row x 128-column tile of x.  Blocks run down columns:
+// output row c of q (= input column c) gets 128 contiguous codes per block.
+// The tile is staged in shared memory as 64 words per row (bf16 pairs), with
+// each 32-row band rotated by 8 words so that the column-wise reads of the
+// four 32-row parts hit 32 distinct banks.
+template <int FMT>
+__global__ void __launch_bounds__(256) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                            int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
+                                                            float* __restrict__ scale, int64_t sld) {
+    __shared__ __align__(16) uint32_t tile[128][64];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int i = threadIdx.x + it * 256;
+        const int rr = i >> 4;
+        const int ch = i & 15;
+        const int64_t c = c0 + ch * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (c < cols) v = __ldcs(reinterpret_cast<const uint4*>(x + (r0 + rr) * ldx + c));
+        const int w = (ch * 4 + 8 * (rr >> 5)) & 63;
+        *reinterpret_cast<uint4*>(&tile[rr][w]) = v;
+    }
+    __syncthreads();
+
+    const int cp = threadIdx.x >> 2;  // column pair 0..63
+    const int p = threadIdx.x & 3;    // 32-row part
+    const int64_t c = c0 + 2 * cp;
+    float lo[32], hi[32];
+    float amax_lo = 0.0f, amax_hi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
+        lo[i] = bf16_lo(w);
+        hi[i] = bf16_hi(w);
+        amax_lo = fmaxf(amax_lo, fabsf(lo[i]));
+        amax_hi = fmaxf(amax_hi, fabsf(hi[i]));
+    }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+        amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
+        amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
+    }
+    float inv_lo, s_lo, inv_hi, s_hi;
+    block_scale<FMT>(amax_lo, inv_lo, s_lo);
+    block_scale<FMT>(amax_hi, inv_hi, s_hi);
+    if (c < cols) {
+        uint32_t wl[8], wh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = Fp8Fmt<FMT>::cvt2(__fmul_rn(lo[4 * i], inv_lo), __fmul_rn(lo[4 * i + 1], inv_lo));
+            const uint32_t b = Fp8Fmt<FMT>::cvt2(__fmul_rn(lo[4 * i + 2], inv_lo), __fmul_rn(lo[4 * i + 3], inv_lo));
+            wl[i] = a | (b << 16);
+            const uint32_t d = Fp8Fmt<FMT>::cvt2(__fmul_rn(hi[4 * i], inv_hi), __fmul_rn(hi[4 * i + 1], inv_hi));
+            const uint32_t e = Fp8Fmt<FMT>::cvt2(__fmul_rn(hi[4 * i + 2], inv_hi), __fmul_rn(hi[4 * i + 3], inv_hi));
+            wh[i] = d | (e << 16);
+        }
+        uint4* dl = reinterpret_cast<uint4*>(q + c * rows + r0 + 32 * p);
+        uint4* dh = reinterpret_cast<uint4*>(q + (c + 1) * rows + r0 + 32 * p);
+        dl[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+        dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+        if (p == 0) {
+            scale[static_cast<int64_t>(blockIdx.y) * sld + c] = s_lo;
+            scale[static_cast<int64_t>(blockIdx.y) * sld + c + 1] = s_hi;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- plain cast
+template <int FMT>
+__global__ void cast_f32_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ q) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 4;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i < n; i += stride) {
+        if (i + 4 <= n) {
+            const float4 v = *reinterpret_cast<const float4*>(x + i);
+            const uint32_t a = Fp8Fmt<FMT>::cvt2(v.x, v.y);
+            const uint32_t b = Fp8Fmt<FMT>::cvt2(v.z, v.w);
+            *reinterpret_cast<uint32_t*>(q + i) = a | (b << 16);
+        } else {
+            for (int64_t k = i; k < n; ++k) q[k] = static_cast<uint8_t>(Fp8Fmt<FMT>::cvt2(x[k], 0.0f) & 0xFF);
+        }
+    }
+}
+
+// -------------------------------------------------------------- host launch
+
+int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                    float* scale, int64_t sld, cudaStream_t stream, int num_sms) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (!transpose) {
+        constexpr int U = 4;
+        const int64_t total = rows * (cols / 128);
+        const int64_t pairs = (total + 1) / 2;
+        int64_t blocks = (pairs + 8 * U - 1) / (8 * U);
+        const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        if (fmt == 0)
+            quantize_rows_kernel<0, U><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(xb, rows, cols, ldx, q,
+                                                                                           scale, sld);
+        else
+            quantize_rows_kernel<1, U><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(xb, rows, cols, ldx, q,
+                                                                                           scale, sld);
+    } else {
+        dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+        if (fmt == 0)
+            quantize_cols_kernel<0><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+        else
+            quantize_cols_kernel<1><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, cudaStream_t stream, int num_sms) {
+    int64_t blocks = (n + 1023) / 1024;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (fmt == 0)
+        cast_f32_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, n, q);
+    else
+        cast_f32_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, n, q);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace fp8ll

@@ -1,0 +1,196 @@
+/*
+ * fp8ll.h -- C ABI of the block-scaled FP8 linear-layer GEMM library (sm_103a).
+ *
+ * The library computes the GEMMs of a training linear layer Y = X W^T + b with
+ * fp8 operands that carry one fp32 scale per row per 128-element block of the
+ * contraction dimension:
+ *
+ *   fp8_quantize        bf16 -> e4m3 / e5m2 codes + block scales
+ *   fp8_gemm_fprop      C = A B^T with bias / tanh-GELU epilogues, bf16 out
+ *   fp8_gemm_dgrad      C = A B^T times gelu'(Z), optional bias-gradient sums
+ *   fp8_gemm_wgrad      fp32 out (+)= A B^T
+ *   fp8_grouped_wgrad   per-group fp32 out_g (+)= A_g B_g^T, groups along K
+ *
+ * Conventions shared by every entry point
+ *   - One row-major "NT" convention: C[M][N] = A[M][K] . B[N][K]^T; both
+ *     operands are K-contiguous ("nt" on "Weight gradient kernels for dense
+ *     and MoE models").  Output features are N, so a bias has length N.
+ *   - Scales are fp32, laid out [K/128][scale_ld]: scale[kb * scale_ld + r] is
+ *     the scale of block kb of row r; scale_ld >= rows and scale_ld % 4 == 0
+ *     (fp8_scale_ld(rows) gives the smallest legal value).
+ *   - All pointers except k_sizes are DEVICE pointers owned by the caller.  The
+ *     library never allocates, frees or synchronizes, except that
+ *     fp8_get_device_status synchronizes the given stream.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).
+ *   - Return value: FP8LL_OK (0) or a negative FP8LL_ERR_* code.  Arguments are
+ *     validated on the host before anything is launched; an invalid call
+ *     launches nothing and leaves every buffer untouched.
+ *   - Kernels never trap.  A pipeline wait that runs past its time budget
+ *     records FP8LL_ERR_TIMEOUT in a device status word, which
+ *     fp8_get_device_status reports.
+ */
+#ifndef FP8LL_H
+#define FP8LL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fp8ll_stream_t; /* same type as cudaStream_t */
+
+/* fp8 formats: e4m3 for the forward GEMM, e5m2 for gradients ("FP8 GEMM for
+ * the fprop should use fast accumulation").  OCP FP8 bit layouts; e4m3 has no
+ * infinity (max 448), e5m2 max 57344. */
+enum { FP8LL_E4M3 = 0, FP8LL_E5M2 = 1 };
+
+/* Epilogues ("Replaced cublasLt calls with rocblas gemm + 6 manually crafted
+ * epilogues": BIAS, GELU and bias-gradient epilogues; bias length is the
+ * output-feature count).
+ *   NONE        fprop: Y = C
+ *   BIAS        fprop: Y = C + bias[j]
+ *   BIAS_GELU   fprop: Z = C + bias[j]; Y = gelu(Z); aux = Z (pre-activation)
+ *   DGELU       dgrad: dZ = C * gelu'(aux)
+ *   DGELU_BGRAD dgrad: dZ as DGELU, and bgrad[j] = sum_i dZ[i][j] (fp32)
+ * gelu is the tanh form 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))). */
+enum {
+    FP8LL_EPI_NONE = 0,
+    FP8LL_EPI_BIAS = 1,
+    FP8LL_EPI_BIAS_GELU = 2,
+    FP8LL_EPI_DGELU = 3,
+    FP8LL_EPI_DGELU_BGRAD = 4
+};
+
+/* Accumulation precision, an explicit per-call flag ("FP8 GEMM for the fprop
+ * should use fast accumulation": DEFAULT = fast, HIGHEST = full).
+ *   FULL: each 128-deep K block's fp32 partial product is promoted into the
+ *         fp32 accumulator with its own scale pair as soon as it is ready.
+ *   FAST: K blocks are promoted in batches (fewer promotion rounds); each
+ *         block still gets its own scale pair. */
+enum { FP8LL_ACC_FULL = 0, FP8LL_ACC_FAST = 1 };
+
+enum {
+    FP8LL_OK = 0,
+    FP8LL_ERR_INVALID_ARG = -1,      /* null / misaligned pointer, bad size, bad enum */
+    FP8LL_ERR_UNSUPPORTED_DEVICE = -2, /* current device is not sm_103 */
+    FP8LL_ERR_LAUNCH = -3,           /* a CUDA launch or driver call failed */
+    FP8LL_ERR_TIMEOUT = -4,          /* a kernel pipeline wait ran out of time */
+    FP8LL_ERR_WORKSPACE = -5         /* workspace missing or too small */
+};
+
+/* One fp8 operand: codes q[rows][ld_q] (row stride ld_q bytes, K contiguous)
+ * and scales scale[K/128][scale_ld].  q and scale must be 16-byte aligned,
+ * ld_q % 16 == 0.  fmt is FP8LL_E4M3 or FP8LL_E5M2. */
+typedef struct {
+    const uint8_t* q;
+    const float* scale;
+    int64_t ld_q;
+    int64_t scale_ld;
+    int32_t fmt;
+    int32_t reserved;
+} fp8ll_operand_t;
+
+/* Smallest legal scale leading dimension for `rows` rows: rows rounded up to
+ * a multiple of 4 (16-byte rows for the TMA engine). */
+int64_t fp8_scale_ld(int64_t rows);
+
+/* Per-128-block cast of a bf16 matrix ("Weight gradient kernels for dense and
+ * MoE models": the per-token cast applied to both operands before the
+ * weight-gradient GEMM).  For each block of 128 values:
+ *   amax = max|x|; inv = fl32(FMAX / amax); scale = fl32(amax / FMAX);
+ *   q = round-to-nearest-even, saturating fp8 encode of fl32(x * inv)
+ * with FMAX = 448 (e4m3) or 57344 (e5m2); a block whose amax is 0, or whose
+ * FMAX / amax overflows fp32, gets inv = scale = 1.
+ *   x:        bf16 [rows][ldx], 16-byte aligned, ldx % 8 == 0, ldx >= cols.
+ *   transpose = 0: blocks run along each row (cols % 128 == 0).
+ *             q [rows][cols] (row stride cols), scale [cols/128][scale_ld],
+ *             scale_ld >= rows.
+ *   transpose = 1: blocks run down each column (rows % 128 == 0,
+ *             cols % 8 == 0).  q is the transposed matrix [cols][rows] (row
+ *             stride rows), scale [rows/128][scale_ld], scale_ld >= cols.
+ *             This produces the K-major operands of the weight-gradient
+ *             GEMM, whose contraction runs over tokens.
+ * rows == 0 or cols == 0 is a no-op. */
+int fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose,
+                 uint8_t* q, float* scale, int64_t scale_ld, fp8ll_stream_t stream);
+
+/* Element-wise fp32 -> fp8 code conversion with the same round-to-nearest-
+ * even, saturating conversion the quantize kernel applies after scaling (no
+ * scaling here).  x, q: device, n elements.  For conformance tests of the
+ * device encoder; NaN inputs give a NaN code. */
+int fp8_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, fp8ll_stream_t stream);
+
+/* Forward GEMM ("Replaced cublasLt calls ...": Y = X W^T + b with X (m,k),
+ * W (n,k), bias of length n; e4m3 operands per "FP8 GEMM for the fprop should
+ * use fast accumulation").
+ *   C[i][j] = sum_kb sA[kb][i] sB[kb][j] sum_{k in kb} qA[i][k] qB[j][k]
+ *   A: M x K operand (X), B: N x K operand (W); K % 128 == 0, K >= 128.
+ *   epi: FP8LL_EPI_NONE, _BIAS or _BIAS_GELU.  bias_bf16: [N] (required for
+ *   BIAS / BIAS_GELU, ignored for NONE).  out_bf16: [M][N] contiguous.
+ *   aux_bf16: [M][N] receives Z = C + bias for BIAS_GELU (may be NULL), unused
+ *   otherwise.  acc_mode: FP8LL_ACC_FULL or _FAST.  M, N >= 1, any value. */
+int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                   const void* bias_bf16, int epi, int acc_mode, void* out_bf16, void* aux_bf16,
+                   fp8ll_stream_t stream);
+
+/* Bytes of workspace fp8_gemm_dgrad needs for FP8LL_EPI_DGELU_BGRAD: one fp32
+ * partial column sum per 128-row band of C, ceil(M/128) * N * 4. */
+size_t fp8_workspace_size(int64_t M, int64_t N);
+
+/* Data-gradient GEMM with the GELU-derivative epilogue ("Replaced cublasLt
+ * calls ...": backward of bias + GELU, derivative first, then the bias
+ * gradient as a column sum in fp32).
+ *   C = A B^T as in fp8_gemm_fprop (A: the incoming gradient, e5m2 typically;
+ *   B: the weight operand).  aux_bf16: Z [M][N], the stored pre-activation.
+ *   out_bf16: dZ = C * gelu'(Z), bf16 [M][N].
+ *   epi = FP8LL_EPI_DGELU_BGRAD also writes bgrad [N] (fp32, length N, the
+ *   sum over all M rows of the fp32 dZ before rounding) using `workspace`
+ *   (device, >= fp8_workspace_size(M, N) bytes, 16-byte aligned); the sum is
+ *   deterministic (fixed order).  epi = FP8LL_EPI_DGELU ignores bgrad and the
+ *   workspace. */
+int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                   const void* aux_bf16, int epi, int acc_mode, void* out_bf16, float* bgrad, void* workspace,
+                   size_t workspace_bytes, fp8ll_stream_t stream);
+
+/* Weight-gradient GEMM ("Weight gradient kernels for dense and MoE models":
+ * fp8 x fp8 -> fp32, out += a b^T).
+ *   out: fp32 [M][N] contiguous, 16-byte aligned.
+ *   accumulate = 1: out[i][j] += C[i][j]  (the page's semantics; calling twice
+ *                   adds twice -- the call is not idempotent)
+ *   accumulate = 0: out[i][j]  = C[i][j]
+ *   K % 128 == 0; K == 0 leaves out unchanged (accumulate = 1) or zeroes it. */
+int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                   float* out, int accumulate, int acc_mode, fp8ll_stream_t stream);
+
+/* k-grouped weight gradient for MoE experts ("Weight gradient kernels for
+ * dense and MoE models", grouped table): group g owns K columns
+ * [off_g, off_g + k_sizes[g]) of both operands, off_g = sum of earlier sizes,
+ * and out_g = out + g * M * N:
+ *   out_g (+)= A[:, off_g : off_g + K_g] . B[:, off_g : off_g + K_g]^T
+ *   k_sizes: HOST array of G values, each >= 0 and % 128 == 0.  A zero-size
+ *   group leaves out_g unchanged (accumulate = 1) or zeroes it.
+ *   1 <= G <= 256.  A.ld_q, B.ld_q >= sum of k_sizes. */
+int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const fp8ll_operand_t* A,
+                      const fp8ll_operand_t* B, float* out, int accumulate, int acc_mode, fp8ll_stream_t stream);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: FP8LL_OK, or the first FP8LL_ERR_TIMEOUT recorded by a
+ * kernel since the last call; FP8LL_ERR_LAUNCH if CUDA reports an error. */
+int fp8_get_device_status(fp8ll_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fp8_status_string(int code);
+
+/* Test hook: for the next launch only, the GEMM producer issues no loads, so
+ * the pipeline waits run out after `budget_ms` milliseconds and the kernel
+ * returns early with FP8LL_ERR_TIMEOUT recorded.  Nothing is written to the
+ * GEMM outputs in that launch.  Returns FP8LL_OK. */
+int fp8_debug_starve_next_gemm(int budget_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8LL_H */

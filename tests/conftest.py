@@ -18,3 +18,16 @@ def oracle_mod():
     import oracle
     oracle._load()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def fp8():
+    """The CUDA library's binding, built in-tree for sm_103a (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_linear_layer_gb300.build as b
+    b.build()
+    import fp8_linear_layer_gb300 as f
+    f.lib()
+    return f

@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads and exports every symbol include/fp8ll.h
+declares; host-side validation rejects bad arguments before any device work.
+CPU only: no call here reaches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fp8ll.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import fp8_linear_layer_gb300.build as b
+    b.build()
+    import fp8_linear_layer_gb300 as f
+    return f.lib()
+
+
+def test_header_declares_the_expected_calls():
+    names = header_functions()
+    for n in ("fp8_quantize", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_grouped_wgrad"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import fp8_linear_layer_gb300 as f
+    names = header_functions()
+    assert sorted(f.EXPORTS) == names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_scale_ld_and_workspace(L):
+    import fp8_linear_layer_gb300 as f
+    assert [f.scale_ld(r) for r in (1, 4, 5, 101, 128)] == [4, 4, 8, 104, 128]
+    assert f.workspace_size(8192, 14336) == 64 * 4 * 14336 * 4
+    assert f.workspace_size(1, 1) == 4 * 4
+    assert f.workspace_size(0, 5) == 0
+
+
+def test_status_strings(L):
+    import fp8_linear_layer_gb300 as f
+    assert f.status_string(0) == "ok"
+    assert "timed out" in f.status_string(-4)
+    assert f.status_string(12345) == "unknown status"
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    import fp8_linear_layer_gb300 as f
+    E = f.binding.ERR_INVALID_ARG
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)  # never dereferenced: validation fails first
+    # quantize: bad format, misaligned pointer, cols not a multiple of 128
+    assert L.fp8_quantize(fake, 4, 128, 128, 7, 0, fake, fake, 4, None) == E
+    assert L.fp8_quantize(vp(0x10002), 4, 128, 128, 0, 0, fake, fake, 4, None) == E
+    assert L.fp8_quantize(fake, 4, 100, 128, 0, 0, fake, fake, 4, None) == E
+    assert L.fp8_quantize(fake, 100, 128, 128, 0, 1, fake, fake, 128, None) == E  # rows % 128 != 0
+    assert L.fp8_quantize(fake, 4, 128, 128, 0, 0, fake, fake, 3, None) == E      # scale_ld too small
+    assert L.fp8_quantize(None, 0, 0, 0, 0, 0, None, None, 0, None) == 0          # empty is a no-op
+    op = f.binding.OperandStruct(0x10000, 0x20000, 256, 8, 0, 0)
+    bad = f.binding.OperandStruct(0x10000, 0x20000, 200, 8, 0, 0)   # ld_q % 16 != 0
+    ob, oo = ctypes.byref(op), ctypes.byref(bad)
+    assert L.fp8_gemm_fprop(8, 8, 256, ob, oo, fake, 2, 0, fake, fake, None) == E
+    assert L.fp8_gemm_fprop(8, 8, 200, ob, ob, fake, 2, 0, fake, fake, None) == E   # K % 128
+    assert L.fp8_gemm_fprop(8, 8, 256, ob, ob, None, 2, 0, fake, fake, None) == E   # bias missing
+    assert L.fp8_gemm_fprop(8, 8, 256, ob, ob, fake, 3, 0, fake, fake, None) == E   # dgrad epilogue
+    assert L.fp8_gemm_fprop(8, 8, 256, ob, ob, fake, 2, 5, fake, fake, None) == E   # bad acc mode
+    assert L.fp8_gemm_fprop(0, 8, 256, ob, ob, fake, 2, 0, fake, fake, None) == E   # M = 0
+    assert L.fp8_gemm_dgrad(8, 8, 256, ob, ob, fake, 4, 0, fake, fake, fake, 4, None) == f.binding.ERR_WORKSPACE
+    assert L.fp8_gemm_dgrad(8, 8, 256, ob, ob, None, 3, 0, fake, None, None, 0, None) == E  # aux missing
+    ks = (ctypes.c_int64 * 2)(128, 100)
+    assert L.fp8_grouped_wgrad(2, 8, 8, ks, ob, ob, fake, 1, 0, None) == E              # K_g % 128
+    ks0 = (ctypes.c_int64 * 1)(128)
+    assert L.fp8_grouped_wgrad(0, 8, 8, ks0, ob, ob, fake, 1, 0, None) == E
+    assert L.fp8_grouped_wgrad(1, 8, 8, ks0, ob, ob, fake, 2, 0, None) == E             # accumulate flag
+    assert L.fp8_debug_starve_next_gemm(0) == E

@@ -1,0 +1,201 @@
+"""GPU GEMMs (through the C ABI) vs the CPU oracle, element by element.
+
+Bounds: |gpu - oracle| <= 2e-3 * S in full accumulation (S = sum_k |a_ik b_jk|
+of the dequantized operands), plus one bf16 ulp for bf16 outputs and one fp32
+ulp for the fp32 read-modify-write.  Epilogue terms propagate through
+|gelu'| <= 1.13.  Shapes span several 128 x 256 tiles with ragged M/N tails.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import FULL_C, MAX_DGELU, assert_within, bf16_to_f64, bf16_ulp, f32_ulp, sample_indices
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = 0, 1
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def quant_both(fp8, a, b, fa, fb):
+    """GPU operands and, independently, the oracle's operands from the same bf16 bytes."""
+    A = fp8.quantize(a.cuda(), fa)
+    B = fp8.quantize(b.cuda(), fb)
+    qa, sa = oracle.quantize(workloads.bits(a), fa)
+    qb, sb = oracle.quantize(workloads.bits(b), fb)
+    return A, B, (qa, sa, fa), (qb, sb, fb)
+
+
+SHAPES = [(256, 256, 256), (1, 1, 128), (300, 520, 384), (129, 257, 128), (640, 1000, 1024), (77, 13, 256),
+          (513, 769, 640)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_fprop_vs_oracle(fp8, M, N, K, epi):
+    x = workloads.normal_bf16((M, K), 11, "x")
+    w = workloads.normal_bf16((N, K), 11, "w")
+    bias = workloads.normal_bf16((N,), 11, "b", std=0.1)
+    A, B, oa, ob = quant_both(fp8, x, w, E4M3, E4M3)
+    Y, Z = fp8.gemm_fprop(A, B, bias.cuda() if epi else None, epi=epi)
+    torch.cuda.synchronize()
+    acc, S = oracle.gemm(*oa, *ob)
+    Zo, Yo = oracle.fprop_epilogue(acc, workloads.bits(bias) if epi else None, gelu_on=(epi == 2))
+    y = bf16_to_f64(Y)
+    gain = MAX_DGELU if epi == 2 else 1.0
+    bound = gain * FULL_C * S + bf16_ulp(np.maximum(np.abs(y), np.abs(Yo))) + 1e-6 * np.abs(Zo)
+    assert_within(y, Yo, bound, "Y")
+    if epi == 2:
+        z = bf16_to_f64(Z)
+        assert_within(z, Zo, FULL_C * S + bf16_ulp(np.maximum(np.abs(z), np.abs(Zo))), "Z")
+
+
+def test_fprop_is_x_times_w_transposed(fp8):
+    # distinct, non-symmetric operands: a transposed or swapped result fails
+    M, N, K = 130, 300, 256
+    x = workloads.normal_bf16((M, K), 5, "x")
+    w = workloads.normal_bf16((N, K), 6, "w") * 3
+    A, B, oa, ob = quant_both(fp8, x, w.to(torch.bfloat16), E4M3, E4M3)
+    Y, _ = fp8.gemm_fprop(A, B, None, epi=0)
+    torch.cuda.synchronize()
+    assert Y.shape == (M, N)
+    acc, S = oracle.gemm(*oa, *ob)
+    y = bf16_to_f64(Y)
+    assert_within(y, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(y), np.abs(acc))), "Y")
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("epi", [3, 4])
+def test_dgrad_vs_oracle(fp8, M, N, K, epi):
+    dy = workloads.normal_bf16((M, K), 21, "dy", std=1e-2)
+    w = workloads.normal_bf16((N, K), 21, "w", std=0.02)
+    z = workloads.normal_bf16((M, N), 21, "z", std=2.0)  # stored pre-activation (seeded input)
+    A, B, oa, ob = quant_both(fp8, dy, w, E5M2, E4M3)
+    dZ, bg = fp8.gemm_dgrad(A, B, z.cuda(), epi=epi)
+    torch.cuda.synchronize()
+    acc, S = oracle.gemm(*oa, *ob)
+    dzo = oracle.dgrad_epilogue(acc, workloads.bits(z))
+    g = np.abs(oracle.dgelu(bf16_to_f64(z)))
+    d = bf16_to_f64(dZ)
+    bound = g * FULL_C * S + bf16_ulp(np.maximum(np.abs(d), np.abs(dzo))) + 1e-6 * np.abs(dzo)
+    assert_within(d, dzo, bound, "dZ")
+    if epi == 4:
+        bgo = oracle.colsum(dzo)
+        n_tiles = (M + 127) // 128
+        bbound = (g * FULL_C * S).sum(axis=0) + (8 + 4 * n_tiles) * 2.0 ** -24 * np.abs(dzo).sum(axis=0) + 1e-30
+        assert bg.shape == (N,)
+        assert_within(bg.cpu().double().numpy(), bgo, bbound, "bgrad")
+
+
+def test_bgrad_closed_form(fp8):
+    # pre-activation 20 -> gelu' == 1 in fp32 too; all-ones operands -> every
+    # dZ entry equals K, every bias-gradient entry M * K (exact in fp32)
+    M, N, K = 300, 270, 256
+    ones_a = torch.ones(M, K, dtype=torch.bfloat16)
+    ones_b = torch.ones(N, K, dtype=torch.bfloat16)
+    A = fp8.quantize(ones_a.cuda(), E5M2)
+    B = fp8.quantize(ones_b.cuda(), E4M3)
+    z = torch.full((M, N), 20.0, dtype=torch.bfloat16, device="cuda")
+    dZ, bg = fp8.gemm_dgrad(A, B, z, epi=4)
+    torch.cuda.synchronize()
+    assert torch.all(torch.abs(dZ.float() - K) <= K * 2.0 ** -8)
+    assert torch.all(torch.abs(bg - M * K) <= M * K * 2.0 ** -20)
+    assert bg.shape == (N,)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES + [(256, 384, 0)])
+@pytest.mark.parametrize("accumulate", [True, False])
+def test_wgrad_vs_oracle(fp8, M, N, K, accumulate):
+    Kq = max(K, 128)
+    a = workloads.normal_bf16((M, Kq), 31, "a", std=0.02)
+    b = workloads.normal_bf16((N, Kq), 31, "b", std=0.02)
+    A, B, oa, ob = quant_both(fp8, a, b, E4M3, E4M3)
+    pre = workloads.normal_f32((M, N), 31, "pre", std=1e-3)
+    out = pre.clone().cuda() if accumulate else torch.full((M, N), float("nan"), device="cuda")
+    fp8.gemm_wgrad(A, B, out, accumulate=accumulate, K=K)
+    torch.cuda.synchronize()
+    if K:
+        acc, S = oracle.gemm(*oa, *ob, K=K)
+    else:
+        acc, S = np.zeros((M, N)), np.zeros((M, N))
+    want = oracle.wgrad(acc, pre.double().numpy() if accumulate else None)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    assert_within(got, want, FULL_C * S + f32_ulp(want), "out")
+    if K == 0 and accumulate:
+        assert np.array_equal(got, pre.double().numpy())
+
+
+def test_wgrad_second_call_doubles(fp8):
+    M, N, K = 300, 520, 512
+    a = workloads.normal_bf16((M, K), 41, "a")
+    b = workloads.normal_bf16((N, K), 41, "b")
+    A, B, oa, ob = quant_both(fp8, a, b, E5M2, E4M3)
+    pre = workloads.normal_f32((M, N), 41, "pre")
+    out = pre.clone().cuda()
+    fp8.gemm_wgrad(A, B, out)
+    once = out.cpu().double().numpy()
+    fp8.gemm_wgrad(A, B, out)
+    twice = out.cpu().double().numpy()
+    acc, S = oracle.gemm(*oa, *ob)
+    p = pre.double().numpy()
+    assert_within(once - p, acc, FULL_C * S + 2 * f32_ulp(once), "first increment")
+    assert_within(twice - p, 2 * acc, 2 * FULL_C * S + 4 * f32_ulp(twice), "second call doubles")
+
+
+def test_worked_example_from_the_page(fp8):
+    """x = ones, y = rand; out pre-filled with the fp32 reference; one call gives
+    out / ref ~ 2 (the page prints 1.9995 .. 2.0009); a zero pre-fill gives ~1."""
+    g = json.load(open(os.path.join(GOLDEN, "deepgemm_wgrad_ones_rand.json")))
+    m, n, k = g["m"], g["n"], g["k"]
+    x = torch.ones(m, k, dtype=torch.bfloat16, device="cuda")
+    y = workloads.uniform_bf16((n, k), 1, "y").cuda()
+    ref = x.float() @ y.float().t()
+    X = fp8.quantize(x, E4M3)
+    Yq = fp8.quantize(y, E4M3)
+    out1 = ref.clone()
+    fp8.gemm_wgrad(X, Yq, out1)
+    ratio = (out1 / ref).cpu().double().numpy()
+    assert np.all(np.abs(ratio - 2.0) <= 2e-3)
+    lo, hi = min(g["printed_ratio_entries"]), max(g["printed_ratio_entries"])
+    assert np.mean((ratio >= lo - 1e-4) & (ratio <= hi + 1e-4)) > 0.5
+    out0 = torch.zeros_like(ref)
+    fp8.gemm_wgrad(X, Yq, out0)
+    r0 = (out0 / ref).cpu().double().numpy()
+    assert np.all(np.abs(r0 - 1.0) <= 2e-3)
+
+
+@pytest.mark.parametrize("accumulate", [True, False])
+def test_grouped_wgrad_vs_oracle(fp8, accumulate):
+    M, N = 300, 520
+    ks = [256, 0, 384, 128, 0]
+    tot = sum(ks)
+    a = workloads.normal_bf16((M, tot), 51, "a", std=0.02)
+    b = workloads.normal_bf16((N, tot), 51, "b", std=0.02)
+    A, B, oa, ob = quant_both(fp8, a, b, E4M3, E4M3)
+    pre = workloads.normal_f32((len(ks), M, N), 51, "pre", std=1e-3)
+    out = pre.clone().cuda() if accumulate else torch.full((len(ks), M, N), float("nan"), device="cuda")
+    fp8.grouped_wgrad(A, B, ks, out, accumulate=accumulate)
+    torch.cuda.synchronize()
+    want, S = oracle.grouped_wgrad(*oa, *ob, ks, prefill=pre.double().numpy() if accumulate else None)
+    got = out.cpu().double().numpy()
+    assert_within(got, want, FULL_C * S + f32_ulp(want), "grouped out")
+    for g, kg in enumerate(ks):
+        if kg == 0:
+            if accumulate:
+                assert np.array_equal(got[g], pre[g].double().numpy())  # bit-identical
+            else:
+                assert np.all(got[g] == 0.0)
+
+
+def test_all_ones_closed_form(fp8):
+    M, N, K = 257, 513, 1024
+    A = fp8.quantize(torch.ones(M, K, dtype=torch.bfloat16, device="cuda"), E4M3)
+    B = fp8.quantize(torch.ones(N, K, dtype=torch.bfloat16, device="cuda"), E4M3)
+    out = torch.zeros(M, N, device="cuda")
+    fp8.gemm_wgrad(A, B, out)
+    assert torch.all(torch.abs(out - K) <= K * 2.0 ** -20)
