@@ -1,0 +1,85 @@
+"""One training step of an FP8 linear layer with bias and tanh-GELU, built
+from the C-ABI calls (no arithmetic here: every step is a library kernel).
+
+Forward and backward follow "Replaced cublasLt calls with rocblas gemm + 6
+manually crafted epilogues" (Y = X W^T + b; dW from the output gradient and
+X; db = column sum of the gradient at the pre-activation, GELU derivative
+first), with e4m3 forward operands and e5m2 gradients ("FP8 GEMM for the fprop
+should use fast accumulation") and the accumulating fp32 weight gradient of
+"Weight gradient kernels for dense and MoE models":
+
+    X  (m x k) --quantize rows, e4m3-->  Xq          W (n x k) --rows, e4m3--> Wq
+    fprop:  Z = Xq Wq^T + b,  Y = gelu(Z)          (bf16, Z kept)
+    dY (m x k) --rows, e5m2--> dYq    (the gradient arriving through the next
+                                       layer's weight, taken to be W^T)
+    dgrad:  dZ = (dYq Wq^T) * gelu'(Z),  db = sum_tokens dZ      (bf16 dZ, fp32 db)
+    dZ^T --quantize down columns, e5m2-->  (n x m)     X^T --columns, e4m3--> (k x m)
+    wgrad:  dW (n x k, fp32) += dZ^T X    (contraction over the m tokens)
+
+All buffers are allocated once (torch) so a step launches 9 kernels and
+allocates nothing; ``step`` can be captured in a CUDA graph.
+"""
+import torch
+
+from . import binding as B
+
+
+class LinearTrainStep:
+    def __init__(self, m: int, k: int, n: int, device="cuda", acc_mode: int = B.ACC_FULL):
+        assert m % 128 == 0 and k % 128 == 0
+        self.m, self.k, self.n = m, k, n
+        self.acc_mode = acc_mode
+        dev = torch.device(device)
+        self.Xq = B.empty_fp8(m, k, B.E4M3, dev)
+        self.Wq = B.empty_fp8(n, k, B.E4M3, dev)
+        self.dYq = B.empty_fp8(m, k, B.E5M2, dev)
+        self.dZTq = B.empty_fp8(n, m, B.E5M2, dev)
+        self.XTq = B.empty_fp8(k, m, B.E4M3, dev)
+        self.Y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.Z = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.dZ = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.db = torch.empty((n,), dtype=torch.float32, device=dev)
+        self.dW = torch.zeros((n, k), dtype=torch.float32, device=dev)
+        self.ws = torch.empty((B.workspace_size(m, n) // 4,), dtype=torch.float32, device=dev)
+
+    @property
+    def gemm_flops(self) -> int:
+        """Algorithmic flops of the three GEMMs of one step (2 m n k each)."""
+        return 3 * 2 * self.m * self.n * self.k
+
+    def forward(self, X, W, b):
+        B.quantize(X, B.E4M3, out=self.Xq)
+        B.quantize(W, B.E4M3, out=self.Wq)
+        B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y, aux=self.Z)
+        return self.Y
+
+    def backward(self, X, dY):
+        B.quantize(dY, B.E5M2, out=self.dYq)
+        B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode, out=self.dZ, bgrad=self.db,
+                     workspace=self.ws)
+        B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)
+        B.quantize(X, B.E4M3, transpose=True, out=self.XTq)
+        B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)
+        return self.dW, self.db
+
+    def step(self, X, W, b, dY):
+        self.forward(X, W, b)
+        return self.backward(X, dY)
+
+    # launch list of one step, for timing each kernel with events
+    def launches(self, X, W, b, dY):
+        return [
+            ("quantize", lambda: B.quantize(X, B.E4M3, out=self.Xq)),
+            ("quantize", lambda: B.quantize(W, B.E4M3, out=self.Wq)),
+            ("gemm", lambda: B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y,
+                                          aux=self.Z)),
+            ("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq)),
+            ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode,
+                                          out=self.dZ, bgrad=self.db, workspace=self.ws)),
+            ("quantize", lambda: B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)),
+            ("quantize", lambda: B.quantize(X, B.E4M3, transpose=True, out=self.XTq)),
+            ("gemm", lambda: B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)),
+        ]
+
+    # 5 quantize + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
+    KERNELS_PER_STEP = 9

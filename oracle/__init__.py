@@ -39,7 +39,9 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # ORACLE_LIB points the pin tests at a deliberately broken copy of the
+        # oracle (tests/test_oracle_mutants.py); normally unset.
+        path = os.environ.get("ORACLE_LIB") or _build.build()
         lib = ctypes.CDLL(path)
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         lib.oracle_fp8_decode_table.argtypes = [i32, vp]
@@ -52,6 +54,7 @@ def _load():
         lib.oracle_bf16_to_f32.restype = ctypes.c_float
         lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_f64_to_bf16_array.argtypes = [vp, i64, vp]
         lib.oracle_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, vp, i64]
         lib.oracle_gemm.argtypes = [i64, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64, i32,
                                     vp, i64, vp, i64, vp, vp]
@@ -108,6 +111,14 @@ def bf16_to_f64(bits) -> np.ndarray:
 
 def f64_to_bf16(v: float) -> int:
     return int(_load().oracle_f64_to_bf16(float(v)))
+
+
+def f64_to_bf16_array(v) -> np.ndarray:
+    """Round float64 values to bf16 (nearest even); returns uint16 bit patterns."""
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_f64_to_bf16_array(_p(v), v.size, _p(out))
+    return out
 
 
 # ------------------------------------------------------------- quantize ----

@@ -168,6 +168,12 @@ uint16_t oracle_f64_to_bf16(double v)
     return (uint16_t)(sign | (uint16_t)((u >> 16) & 0x7FFF));
 }
 
+void oracle_f64_to_bf16_array(const double* v, int64_t n, uint16_t* out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16(v[i]);
+}
+
 /* ------------------------------------------------------------------------ */
 /* per-128-block quantization ([P3] per-token cast; e4m3/e5m2 from [P4])      */
 /* ------------------------------------------------------------------------ */

@@ -32,6 +32,7 @@ void    oracle_fp8_encode_array(int fmt, const float* x, int64_t n, uint8_t* q);
 /* bf16 helpers (bit patterns stored as uint16) */
 float    oracle_bf16_to_f32(uint16_t h);
 uint16_t oracle_f64_to_bf16(double v); /* round to nearest even, via exact comparison */
+void     oracle_f64_to_bf16_array(const double* v, int64_t n, uint16_t* out);
 
 /* per-128-block quantization (the page's per-token cast) */
 void oracle_quantize(int fmt, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,

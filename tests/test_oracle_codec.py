@@ -100,6 +100,8 @@ def test_bf16_helpers(oracle_mod):
     for v in x.numpy()[:2000]:  # fp32 inputs: torch's fp32 -> bf16 cast is single rounding
         want = int(torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[0])
         assert oracle_mod.f64_to_bf16(float(v)) == want
+    arr = oracle_mod.f64_to_bf16_array(x.numpy()[:2000].astype(np.float64))
+    assert [int(a) for a in arr] == [oracle_mod.f64_to_bf16(float(v)) for v in x.numpy()[:2000]]
     # tie to even: 1 + 2^-8 is halfway between 1 and 1 + 2^-7
     assert oracle_mod.f64_to_bf16(1.0 + 2.0 ** -8) == 0x3F80
     assert oracle_mod.f64_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82
