@@ -102,37 +102,41 @@ __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu
 // ------------------------------------------------------------------ stores
 
 // wgrad: out (+)= acc, fp32
+// out += acc is a single fp32 add per element, done in L2 by a vector
+// reduction (no load round trip; each element receives exactly one add per
+// call, so the result is deterministic).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, int r, int cbase,
-                                            float (&acc)[kHalfN]) {
+                                            float2 (&acc)[kHalfN / 2]) {
     if (r >= p.M) return;
     float* orow = static_cast<float*>(p.out) + (static_cast<int64_t>(out_index) * p.M + r) * p.N + cbase;
     if ((p.N & 3) == 0 && cbase + kHalfN <= p.N) {
         if (p.accumulate) {
 #pragma unroll
-            for (int j = 0; j < kHalfN; j += 4) {
-                float4 o = *reinterpret_cast<const float4*>(orow + j);
-                o.x += acc[j];
-                o.y += acc[j + 1];
-                o.z += acc[j + 2];
-                o.w += acc[j + 3];
-                *reinterpret_cast<float4*>(orow + j) = o;
-            }
+            for (int j = 0; j < kHalfN; j += 4)
+                red_add_v4(orow + j, acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
         } else {
 #pragma unroll
             for (int j = 0; j < kHalfN; j += 4)
-                *reinterpret_cast<float4*>(orow + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                *reinterpret_cast<float4*>(orow + j) =
+                    make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
         }
     } else {
 #pragma unroll
         for (int j = 0; j < kHalfN; ++j) {
-            if (cbase + j < p.N) orow[j] = (p.accumulate ? orow[j] : 0.0f) + acc[j];
+            const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+            if (cbase + j < p.N) orow[j] = (p.accumulate ? orow[j] : 0.0f) + v;
         }
     }
 }
 
 // fprop: Z = acc + bias[j]; Y = gelu(Z) or Z; bf16 out (+ bf16 aux Z)
 template <int EPI>
-__device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbase, float (&acc)[kHalfN]) {
+__device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbase, float2 (&acc)[kHalfN / 2]) {
     if (r >= p.M) return;
     const int64_t off = static_cast<int64_t>(r) * p.N + cbase;
     uint16_t* out = static_cast<uint16_t*>(p.out) + off;
@@ -144,14 +148,17 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbas
             float z[8];
             if (EPI == kEpiNone) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) z[i] = acc[j + i];
+                for (int i = 0; i < 4; ++i) {
+                    z[2 * i] = acc[j / 2 + i].x;
+                    z[2 * i + 1] = acc[j / 2 + i].y;
+                }
             } else {
                 const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + j));
                 const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    z[2 * i] = acc[j + 2 * i] + bf16_lo(bw[i]);
-                    z[2 * i + 1] = acc[j + 2 * i + 1] + bf16_hi(bw[i]);
+                    z[2 * i] = acc[j / 2 + i].x + bf16_lo(bw[i]);
+                    z[2 * i + 1] = acc[j / 2 + i].y + bf16_hi(bw[i]);
                 }
             }
             uint32_t yw[4];
@@ -173,7 +180,7 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbas
 #pragma unroll
         for (int j = 0; j < kHalfN; ++j) {
             if (cbase + j < p.N) {
-                float z = acc[j];
+                float z = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
                 if (EPI != kEpiNone) z += __uint_as_float(static_cast<uint32_t>(bias[j]) << 16);
                 const float y = (EPI == kEpiBiasGelu) ? gelu_tanh(z) : z;
                 out[j] = static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu);
@@ -185,10 +192,10 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbas
 
 // dgrad: dZ = acc * gelu'(Z); bf16 out.  acc is overwritten with the fp32 dZ
 // (zero outside the matrix) for the bias-gradient sums.
-__device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbase, float (&acc)[kHalfN]) {
+__device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbase, float2 (&acc)[kHalfN / 2]) {
     if (r >= p.M) {
 #pragma unroll
-        for (int j = 0; j < kHalfN; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < kHalfN / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
         return;
     }
     const int64_t off = static_cast<int64_t>(r) * p.N + cbase;
@@ -202,10 +209,9 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
             uint32_t ow[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float d0 = acc[j + 2 * i] * dgelu_tanh(bf16_lo(zw[i]));
-                const float d1 = acc[j + 2 * i + 1] * dgelu_tanh(bf16_hi(zw[i]));
-                acc[j + 2 * i] = d0;
-                acc[j + 2 * i + 1] = d1;
+                const float d0 = acc[j / 2 + i].x * dgelu_tanh(bf16_lo(zw[i]));
+                const float d1 = acc[j / 2 + i].y * dgelu_tanh(bf16_hi(zw[i]));
+                acc[j / 2 + i] = make_float2(d0, d1);
                 ow[i] = pack_bf16x2(d0, d1);
             }
             *reinterpret_cast<uint4*>(out + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -213,13 +219,14 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
     } else {
 #pragma unroll
         for (int j = 0; j < kHalfN; ++j) {
+            float& a = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
             if (cbase + j < p.N) {
                 const float z = __uint_as_float(static_cast<uint32_t>(zp[j]) << 16);
-                const float d = acc[j] * dgelu_tanh(z);
-                acc[j] = d;
+                const float d = a * dgelu_tanh(z);
+                a = d;
                 out[j] = static_cast<uint16_t>(pack_bf16x2(d, 0.0f) & 0xFFFFu);
             } else {
-                acc[j] = 0.0f;
+                a = 0.0f;
             }
         }
     }
@@ -229,18 +236,42 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
 // a butterfly that halves the column set at each step.  Afterwards lane l
 // holds the sum for column l.  The summation order is fixed, so results are
 // deterministic.
-__device__ __forceinline__ float warp_column_sum32(float (&v)[kHalfN], int c0, int lane) {
+template <int C0>
+__device__ __forceinline__ float warp_column_sum32(const float2 (&acc)[kHalfN / 2], int lane) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[2 * i] = acc[C0 / 2 + i].x;
+        v[2 * i + 1] = acc[C0 / 2 + i].y;
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int i = 0; i < off; ++i) {
-            const float send = upper ? v[c0 + i] : v[c0 + i + off];
-            const float keep = upper ? v[c0 + i + off] : v[c0 + i];
-            v[c0 + i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    return v[c0];
+    return v[0];
+}
+
+// acc[C*16 .. C*16+15] += P[r0 .. r0+31] * (sA * sB[C*32 .. C*32+31]), two columns per
+// packed fp32x2 multiply / fma (each rounded to nearest, as a scalar mul + fma).
+template <int C>
+__device__ __forceinline__ void promote_chunk(float2 (&acc)[kHalfN / 2], const uint32_t (&r)[64], int r0,
+                                              float2 sa2, const float* sbp) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 sb4 = *reinterpret_cast<const float4*>(sbp + C * 32 + j);
+        const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
+        const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
+        const int a = (C * 32 + j) / 2;
+        acc[a] = __ffma2_rn(make_float2(__uint_as_float(r[r0 + j]), __uint_as_float(r[r0 + j + 1])), s01, acc[a]);
+        acc[a + 1] =
+            __ffma2_rn(make_float2(__uint_as_float(r[r0 + j + 2]), __uint_as_float(r[r0 + j + 3])), s23, acc[a + 1]);
+    }
 }
 
 // -------------------------------------------------------------------- kernel
@@ -407,38 +438,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_tile(p, t, g, mt, nt);
             const GroupEntry ge = p.groups[g];
             const int m0 = mt * kBM, n0 = nt * kBN;
-            float acc[kHalfN];
+            float2 acc[kHalfN / 2];
 #pragma unroll
-            for (int j = 0; j < kHalfN; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < kHalfN / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
             for (int kb = 0; kb < ge.nkb; ++kb) {
                 ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
                 if (ok) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
                 if (!ok) break;
                 tc_fence_after();
                 const float sa = sm.sa[ss][row];
+                const float2 sa2 = make_float2(sa, sa);
                 const float* sbp = &sm.sb[ss][half * kHalfN];
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(ab * kBN + half * kHalfN);
-#pragma unroll
-                for (int c = 0; c < kHalfN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 sb4 = *reinterpret_cast<const float4*>(sbp + c * 32 + j);
-                        acc[c * 32 + j + 0] = fmaf(__uint_as_float(r[j + 0]), sa * sb4.x, acc[c * 32 + j + 0]);
-                        acc[c * 32 + j + 1] = fmaf(__uint_as_float(r[j + 1]), sa * sb4.y, acc[c * 32 + j + 1]);
-                        acc[c * 32 + j + 2] = fmaf(__uint_as_float(r[j + 2]), sa * sb4.z, acc[c * 32 + j + 2]);
-                        acc[c * 32 + j + 3] = fmaf(__uint_as_float(r[j + 3]), sa * sb4.w, acc[c * 32 + j + 3]);
-                    }
-                }
+                uint32_t r[64];
+                tmem_ld_32x32b_x64_sync(tbase, r);
+                promote_chunk<0>(acc, r, 0, sa2, sbp);
+                promote_chunk<1>(acc, r, 32, sa2, sbp);
+                tmem_ld_32x32b_x64_sync(tbase + 64, r);
+                // every TMEM read of this buffer is complete: hand it back to the MMA warp
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                    mbar_arrive(smem_addr(&sm.sempty[ss]));
-                }
+                if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+                promote_chunk<2>(acc, r, 0, sa2, sbp);
+                promote_chunk<3>(acc, r, 32, sa2, sbp);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
                 ring_advance<2>(ab, aph);
                 ring_advance<kSStages>(ss, sph);
             }
@@ -454,12 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (EPI == kEpiDgeluBgrad) {
                     // partial column sums of this warp's 32 rows -> workspace band (4*mt + q)
                     float* band = p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N;
-#pragma unroll
-                    for (int c = 0; c < kHalfN / 32; ++c) {
-                        const float v = warp_column_sum32(acc, c * 32, lane);
-                        const int col = cbase + c * 32 + lane;
-                        if (col < p.N) band[col] = v;
-                    }
+                    const float v0 = warp_column_sum32<0>(acc, lane);
+                    const float v1 = warp_column_sum32<32>(acc, lane);
+                    const float v2 = warp_column_sum32<64>(acc, lane);
+                    const float v3 = warp_column_sum32<96>(acc, lane);
+                    if (cbase + lane < p.N) band[cbase + lane] = v0;
+                    if (cbase + 32 + lane < p.N) band[cbase + 32 + lane] = v1;
+                    if (cbase + 64 + lane < p.N) band[cbase + 64 + lane] = v2;
+                    if (cbase + 96 + lane < p.N) band[cbase + 96 + lane] = v3;
                 }
             }
         }
