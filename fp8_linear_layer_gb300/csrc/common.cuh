@@ -19,17 +19,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // tanh-form GELU and its derivative ("Replaced cublasLt calls with rocblas
 // gemm + 6 manually crafted epilogues": GELU epilogue in the forward pass,
 // its derivative in the backward pass), evaluated in fp32.
+//   gelu(z)  = 0.5 z (1 + tanh(u)),  u = sqrt(2/pi) (z + 0.044715 z^3)
+//   gelu'(z) = 0.5 (1 + tanh u) + 0.5 z (1 - tanh^2 u) sqrt(2/pi) (1 + 3 * 0.044715 z^2)
+// written with the logistic identities 0.5 (1 + tanh u) = s(2u) and
+// 1 - tanh^2 u = 4 s(2u) s(-2u), s(x) = 1 / (1 + e^-x): the same functions,
+// but without the cancellation of 1 + tanh u for large negative z, so both
+// keep their relative accuracy everywhere.  2u is clamped to +-80, where s is
+// already 0 / 1 to fp32 precision relative to the other term.
 __device__ __forceinline__ float gelu_tanh(float z) {
-    const float c = 0.7978845608028654f;  // sqrt(2/pi)
-    const float u = c * (z + 0.044715f * z * z * z);
-    return 0.5f * z * (1.0f + tanhf(u));
+    const float c2 = 1.5957691216057308f;  // 2 sqrt(2/pi)
+    const float x = fminf(fmaxf(c2 * (z + 0.044715f * z * z * z), -80.0f), 80.0f);
+    return z / (1.0f + expf(-x));
 }
 
 __device__ __forceinline__ float dgelu_tanh(float z) {
-    const float c = 0.7978845608028654f;
+    const float c = 0.7978845608028654f;  // sqrt(2/pi)
     const float z2 = z * z;
-    const float t = tanhf(c * (z + 0.044715f * z2 * z));
-    return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * c * (1.0f + 3.0f * 0.044715f * z2);
+    const float x = fminf(fmaxf(2.0f * c * (z + 0.044715f * z2 * z), -80.0f), 80.0f);
+    const float e = expf(-x);
+    const float sp = 1.0f / (1.0f + e);  // s(2u)
+    const float sm = e * sp;             // s(-2u)
+    return sp + 2.0f * z * c * (1.0f + 3.0f * 0.044715f * z2) * sp * sm;
 }
 
 __device__ __forceinline__ void record_status(int* status, int code) {

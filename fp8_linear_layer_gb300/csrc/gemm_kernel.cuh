@@ -190,60 +190,11 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbas
     }
 }
 
-// dgrad: dZ = acc * gelu'(Z); bf16 out.  acc is overwritten with the fp32 dZ
-// (zero outside the matrix) for the bias-gradient sums.
-__device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbase, float2 (&acc)[kHalfN / 2]) {
-    if (r >= p.M) {
-#pragma unroll
-        for (int j = 0; j < kHalfN / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-        return;
-    }
-    const int64_t off = static_cast<int64_t>(r) * p.N + cbase;
-    uint16_t* out = static_cast<uint16_t*>(p.out) + off;
-    const uint16_t* zp = static_cast<const uint16_t*>(p.aux) + off;
-    if ((p.N & 7) == 0 && cbase + kHalfN <= p.N) {
-#pragma unroll
-        for (int j = 0; j < kHalfN; j += 8) {
-            const uint4 zv = *reinterpret_cast<const uint4*>(zp + j);
-            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-            uint32_t ow[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float d0 = acc[j / 2 + i].x * dgelu_tanh(bf16_lo(zw[i]));
-                const float d1 = acc[j / 2 + i].y * dgelu_tanh(bf16_hi(zw[i]));
-                acc[j / 2 + i] = make_float2(d0, d1);
-                ow[i] = pack_bf16x2(d0, d1);
-            }
-            *reinterpret_cast<uint4*>(out + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kHalfN; ++j) {
-            float& a = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-            if (cbase + j < p.N) {
-                const float z = __uint_as_float(static_cast<uint32_t>(zp[j]) << 16);
-                const float d = a * dgelu_tanh(z);
-                a = d;
-                out[j] = static_cast<uint16_t>(pack_bf16x2(d, 0.0f) & 0xFFFFu);
-            } else {
-                a = 0.0f;
-            }
-        }
-    }
-}
-
 // Column sums of 32 consecutive columns over the 32 rows held by a warp:
 // a butterfly that halves the column set at each step.  Afterwards lane l
 // holds the sum for column l.  The summation order is fixed, so results are
 // deterministic.
-template <int C0>
-__device__ __forceinline__ float warp_column_sum32(const float2 (&acc)[kHalfN / 2], int lane) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v[2 * i] = acc[C0 / 2 + i].x;
-        v[2 * i + 1] = acc[C0 / 2 + i].y;
-    }
+__device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         const bool upper = (lane & off) != 0;
@@ -255,6 +206,56 @@ __device__ __forceinline__ float warp_column_sum32(const float2 (&acc)[kHalfN / 
         }
     }
     return v[0];
+}
+
+// dgrad: dZ = acc * gelu'(Z) -> bf16 out, 32 columns at a time.  With BGRAD,
+// each 32-column chunk's fp32 dZ (zero outside the matrix) is summed over the
+// warp's 32 rows and written to the workspace band of this warp.
+template <bool BGRAD>
+__device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbase, float2 (&acc)[kHalfN / 2],
+                                            float* band, int lane) {
+    const bool row_ok = r < p.M;
+    const int64_t off = static_cast<int64_t>(row_ok ? r : 0) * p.N + cbase;
+    uint16_t* out = static_cast<uint16_t*>(p.out) + off;
+    const uint16_t* zp = static_cast<const uint16_t*>(p.aux) + off;
+    const bool vec = (p.N & 7) == 0 && cbase + kHalfN <= p.N;
+#pragma unroll
+    for (int c = 0; c < kHalfN / 32; ++c) {
+        float v[32];
+        if (row_ok && vec) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                const uint4 zv = *reinterpret_cast<const uint4*>(zp + c * 32 + j);
+                const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a = acc[(c * 32 + j) / 2 + i];
+                    v[j + 2 * i] = a.x * dgelu_tanh(bf16_lo(zw[i]));
+                    v[j + 2 * i + 1] = a.y * dgelu_tanh(bf16_hi(zw[i]));
+                    ow[i] = pack_bf16x2(v[j + 2 * i], v[j + 2 * i + 1]);
+                }
+                *reinterpret_cast<uint4*>(out + c * 32 + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int col = cbase + c * 32 + j;
+                const float a = (j & 1) ? acc[(c * 32 + j) / 2].y : acc[(c * 32 + j) / 2].x;
+                v[j] = 0.0f;
+                if (row_ok && col < p.N) {
+                    const float z = __uint_as_float(static_cast<uint32_t>(zp[c * 32 + j]) << 16);
+                    v[j] = a * dgelu_tanh(z);
+                    out[c * 32 + j] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
+                }
+            }
+        }
+        if (BGRAD) {
+            const float s = warp_column_sum32(v, lane);
+            const int col = cbase + c * 32 + lane;
+            if (col < p.N) band[col] = s;
+        }
+    }
 }
 
 // acc[C*16 .. C*16+15] += P[r0 .. r0+31] * (sA * sB[C*32 .. C*32+31]), two columns per
@@ -475,19 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (EPI == kEpiNone || EPI == kEpiBias || EPI == kEpiBiasGelu) {
                 store_fprop<EPI>(p, r, cbase, acc);
             } else {
-                store_dgrad(p, r, cbase, acc);
-                if (EPI == kEpiDgeluBgrad) {
-                    // partial column sums of this warp's 32 rows -> workspace band (4*mt + q)
-                    float* band = p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N;
-                    const float v0 = warp_column_sum32<0>(acc, lane);
-                    const float v1 = warp_column_sum32<32>(acc, lane);
-                    const float v2 = warp_column_sum32<64>(acc, lane);
-                    const float v3 = warp_column_sum32<96>(acc, lane);
-                    if (cbase + lane < p.N) band[cbase + lane] = v0;
-                    if (cbase + 32 + lane < p.N) band[cbase + 32 + lane] = v1;
-                    if (cbase + 64 + lane < p.N) band[cbase + 64 + lane] = v2;
-                    if (cbase + 96 + lane < p.N) band[cbase + 96 + lane] = v3;
-                }
+                // bias-gradient partials of this warp's 32 rows -> workspace band (4*mt + q)
+                float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
+                                                      : nullptr;
+                store_dgrad<EPI == kEpiDgeluBgrad>(p, r, cbase, acc, band, lane);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
