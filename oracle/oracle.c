@@ -27,7 +27,8 @@
  *    128-element block, amax = max|x|, inv = fl32(FMAX/amax),
  *    scale = fl32(amax/FMAX), q = enc(fl32(x*inv)).  A block whose amax is 0,
  *    or whose FMAX/amax overflows binary32, gets scale = 1, inv = 1.
- *  - GELU is the tanh form 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3))).
+ *  - GELU is the tanh form 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3))),
+ *    evaluated through the identity 0.5 (1 + tanh u) = 1 / (1 + exp(-2u)).
  */
 #include "oracle.h"
 
@@ -286,21 +287,26 @@ void oracle_gemm(int64_t K, int64_t k0,
 /* epilogue math ([P1]: bias, GELU, dGELU, db = column sum)                  */
 /* ------------------------------------------------------------------------ */
 
-/* gelu(z) = 0.5 z (1 + tanh(c (z + 0.044715 z^3))), c = sqrt(2/pi) */
+/* gelu(z) = 0.5 z (1 + tanh(u)), u = c (z + 0.044715 z^3), c = sqrt(2/pi).
+ * Evaluated through 0.5 (1 + tanh u) = 1 / (1 + exp(-2u)): the same number,
+ * without the cancellation of 1 + tanh(u) in binary64 when u < -18. */
 double oracle_gelu(double z)
 {
     const double c = sqrt(2.0 / acos(-1.0));
     const double u = c * (z + 0.044715 * z * z * z);
-    return 0.5 * z * (1.0 + tanh(u));
+    return z / (1.0 + exp(-2.0 * u));
 }
 
-/* d/dz of the above: 0.5 (1 + t) + 0.5 z (1 - t^2) c (1 + 3 * 0.044715 z^2) */
+/* d/dz of the above: 0.5 (1 + t) + 0.5 z (1 - t^2) c (1 + 3 * 0.044715 z^2),
+ * t = tanh(u), with 0.5 (1 + t) = s(2u) and 1 - t^2 = 4 s(2u) s(-2u),
+ * s(x) = 1 / (1 + exp(-x)). */
 double oracle_dgelu(double z)
 {
     const double c = sqrt(2.0 / acos(-1.0));
     const double u = c * (z + 0.044715 * z * z * z);
-    const double t = tanh(u);
-    return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * z * z);
+    const double sp = 1.0 / (1.0 + exp(-2.0 * u));
+    const double sm = 1.0 / (1.0 + exp(2.0 * u));
+    return sp + 2.0 * z * c * (1.0 + 3.0 * 0.044715 * z * z) * sp * sm;
 }
 
 void oracle_gelu_array(const double* z, double* y, int64_t n)

@@ -40,6 +40,35 @@ def test_gelu_matches_torch_tanh_gelu(oracle_mod):
     assert np.max(np.abs(oracle_mod.dgelu(z.numpy()) - zz.grad.numpy())) < 1e-13
 
 
+def _tanh_form_decimal(z, deriv):
+    """gelu / gelu' in the tanh form, 150 significant digits (decimal module)."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 150
+    pi = Decimal("3.14159265358979323846264338327950288419716939937510582097494459230781640628620899862803482534211706798214808651328230664709384460955058223172535940812848111745")
+    c = (Decimal(2) / pi).sqrt()
+    a = Decimal("0.044715")
+    zd = Decimal(repr(float(z)))
+    u = c * (zd + a * zd ** 3)
+    e2 = (2 * u).exp()
+    t = (e2 - 1) / (e2 + 1)
+    if not deriv:
+        return float(Decimal("0.5") * zd * (1 + t))
+    return float(Decimal("0.5") * (1 + t) + Decimal("0.5") * zd * (1 - t * t) * c * (1 + 3 * a * zd * zd))
+
+
+def test_gelu_relative_accuracy_against_150_digit_tanh_form(oracle_mod):
+    # includes large negative z, where 1 + tanh(u) cancels in binary64
+    zs = np.concatenate([np.linspace(-12, 12, 241), [-9.7, -8.3, -7.1, -6.6, 7.3]])
+    g = oracle_mod.gelu(zs)
+    d = oracle_mod.dgelu(zs)
+    for z, gv, dv in zip(zs, g, d):
+        gr = _tanh_form_decimal(z, False)
+        dr = _tanh_form_decimal(z, True)
+        assert abs(gv - gr) <= 1e-13 * abs(gr) + 1e-300
+        # gelu' crosses zero near z = -0.7518: relative there, absolute 1e-15 near it
+        assert abs(dv - dr) <= 1e-12 * abs(dr) + 1e-15
+
+
 def test_max_dgelu_bound(oracle_mod):
     # the error-propagation bound uses max |gelu'| < 1.13
     z = np.linspace(-10, 10, 200001)

@@ -35,11 +35,13 @@ MUTANTS = {
                                                 "const float y = v[k] / inv; /* binary32 product */"),
     "transposed quantize reads rows": ("v[k] = oracle_bf16_to_f32(x[(b * 128 + k) * ldx + c]);",
                                        "v[k] = oracle_bf16_to_f32(x[(b * 128 + k) * ldx + (c % 2)]);"),
-    "gelu wrong sign": ("return 0.5 * z * (1.0 + tanh(u));", "return 0.5 * z * (1.0 - tanh(u));"),
+    "gelu wrong sign": ("return z / (1.0 + exp(-2.0 * u));", "return z / (1.0 + exp(2.0 * u));"),
     "gelu drops the cubic term": ("const double u = c * (z + 0.044715 * z * z * z);\n    return",
                                   "const double u = c * z;\n    return"),
-    "dgelu drops a term": ("return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * z * z);",
-                           "return 0.5 * (1.0 + t);"),
+    "dgelu drops a term": ("return sp + 2.0 * z * c * (1.0 + 3.0 * 0.044715 * z * z) * sp * sm;",
+                           "return sp;"),
+    "dgelu drops the cubic factor": ("return sp + 2.0 * z * c * (1.0 + 3.0 * 0.044715 * z * z) * sp * sm;",
+                                     "return sp + 2.0 * z * c * sp * sm;"),
     "colsum over the wrong axis": ("for (int64_t i = 0; i < M; ++i) s += dz[i * N + j];",
                                    "for (int64_t i = 0; i < M; ++i) s += dz[j * M + i] * (j * M + i < M * N);"),
     "bf16 rounding truncates": ("const double r = nearbyint(a / spacing) * spacing;",
