@@ -45,6 +45,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--acc", choices=["full", "fast"], default="full")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
+    ap.add_argument("--k", type=int, default=K_IN, help="in-features")
+    ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
     return ap.parse_args()
 
 
@@ -64,13 +68,12 @@ def peaks():
         return 1900.0 * FP8_OVER_BF16, 6800.0, "of fallback"
 
 
-def inputs(device):
-    import torch
+def inputs(device, m=M_TOK, k=K_IN, n=N_OUT):
     import workloads
-    X = workloads.normal_bf16((M_TOK, K_IN), SEED, "X")
-    W = workloads.normal_bf16((N_OUT, K_IN), SEED, "W", std=0.02)
-    b = workloads.normal_bf16((N_OUT,), SEED, "b", std=0.02)
-    dY = workloads.normal_bf16((M_TOK, K_IN), SEED, "dY", std=1e-2)
+    X = workloads.normal_bf16((m, k), SEED, "X")
+    W = workloads.normal_bf16((n, k), SEED, "W", std=0.02)
+    b = workloads.normal_bf16((n,), SEED, "b", std=0.02)
+    dY = workloads.normal_bf16((m, k), SEED, "dY", std=1e-2)
     host = [t.pin_memory() for t in (X, W, b, dY)] if device.type == "cuda" else [X, W, b, dY]
     return host
 
@@ -208,6 +211,43 @@ def run_reference(args):
     return 0
 
 
+def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
+    """The same step through the public API with host buffers: each step copies
+    X, W, b, dY from pinned host memory and reads dW, db back."""
+    import torch
+    hX, hW, hb, hdY = host
+    X, W, b, dY = dev_in
+    flops_step = step.gemm_flops
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h_dW = torch.empty(step.dW.shape, dtype=torch.float32).pin_memory()
+    h_db = torch.empty(step.db.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        X.copy_(hX, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        b.copy_(hb, non_blocking=True)
+        dY.copy_(hdY, non_blocking=True)
+        step.step(X, W, b, dY)
+        h_dW.copy_(step.dW, non_blocking=True)
+        h_db.copy_(step.db, non_blocking=True)
+    ev1.record(stream)
+    ev1.synchronize()
+    e2e_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hb, hdY))
+    d2h = h_dW.numel() * 4 + h_db.numel() * 4
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
+    return {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps}
+
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -224,9 +264,11 @@ def run_ours(args):
     fp8.lib()
     acc_mode = fp8.ACC_FAST if args.acc == "fast" else fp8.ACC_FULL
 
-    hX, hW, hb, hdY = inputs(dev)
+    m, k, n = args.m, args.k, args.n
+    default_size = (m, k, n) == (M_TOK, K_IN, N_OUT)
+    hX, hW, hb, hdY = inputs(dev, m, k, n)
     X, W, b, dY = (t.to(dev, non_blocking=True) for t in (hX, hW, hb, hdY))
-    step = LinearTrainStep(M_TOK, K_IN, N_OUT, dev, acc_mode)
+    step = LinearTrainStep(m, k, n, dev, acc_mode)
     launches = step.launches(X, W, b, dY)
     stream = torch.cuda.current_stream()
 
@@ -280,39 +322,16 @@ def run_ours(args):
     flops_step = step.gemm_flops
     value = world * flops_step * args.steps / (ms / 1e3) / 1e12
     fp8_peak, hbm_peak, peak_src = peaks()
-    per_gemm_flops = 2 * M_TOK * N_OUT * K_IN
+    per_gemm_flops = 2 * m * n * k
     avg_gemm_ms = sum(gemm_ms) / len(gemm_ms)
     achieved = per_gemm_flops / (avg_gemm_ms / 1e3) / 1e12
 
     # ------------------------------------------------ end to end (host buffers)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h_dW = torch.empty(step.dW.shape, dtype=torch.float32).pin_memory()
-    h_db = torch.empty(step.db.shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
-    barrier()
-    ev0.record(stream)
-    for _ in range(e2e_steps):
-        X.copy_(hX, non_blocking=True)
-        W.copy_(hW, non_blocking=True)
-        b.copy_(hb, non_blocking=True)
-        dY.copy_(hdY, non_blocking=True)
-        step.step(X, W, b, dY)
-        h_dW.copy_(step.dW, non_blocking=True)
-        h_db.copy_(step.db, non_blocking=True)
-    ev1.record(stream)
-    ev1.synchronize()
-    e2e_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hb, hdY))
-    d2h = h_dW.numel() * 4 + h_db.numel() * 4
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
-
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, step, (hX, hW, hb, hdY), (X, W, b, dY), stream, barrier, world, dev)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and default_size:
         v, dt, cores, sample = cpu_baseline_sample()
         cpu = {"value": v, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
@@ -322,7 +341,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8(e4m3/e5m2) x fp8 -> fp32 accumulate", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "m_tokens": M_TOK, "k_in": K_IN, "n_out": N_OUT,
+            "config": {"workload": WORKLOAD if default_size else "linear_train_step_m%d_k%d_n%d_bias_gelu" % (m, k, n),
+                       "m_tokens": m, "k_in": k, "n_out": n,
                        "acc_mode": args.acc, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
@@ -330,8 +350,7 @@ def run_ours(args):
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),
                          "traffic": None, "avg_gemm_ms": avg_gemm_ms},
-            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
+            "e2e": e2e,
             "gpu_launches": step.KERNELS_PER_STEP * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
