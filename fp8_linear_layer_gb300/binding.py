@@ -23,7 +23,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSP
 
 # every symbol include/fp8ll.h declares
 EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
-           "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
+           "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
            "fp8_status_string", "fp8_debug_starve_next_gemm")
 
 
@@ -59,13 +59,15 @@ def lib():
         L.fp8_workspace_size.argtypes = [i64, i64]
         L.fp8_workspace_size.restype = sz
         L.fp8_gemm_dgrad.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp, sz, vp]
+        L.fp8_gemm_dgrad_noalloc.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp]
         L.fp8_gemm_wgrad.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp]
         L.fp8_grouped_wgrad.argtypes = [i32, i64, i64, ctypes.POINTER(ctypes.c_int64), op, op, vp, i32, i32, vp]
         L.fp8_get_device_status.argtypes = [vp]
         L.fp8_status_string.argtypes = [i32]
         L.fp8_status_string.restype = ctypes.c_char_p
         L.fp8_debug_starve_next_gemm.argtypes = [i32]
-        for name in ("fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_wgrad",
+        for name in ("fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
+                     "fp8_gemm_wgrad",
                      "fp8_grouped_wgrad", "fp8_get_device_status", "fp8_debug_starve_next_gemm"):
             getattr(L, name).restype = i32
         _lib = L

@@ -155,6 +155,25 @@ int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
                    const void* aux_bf16, int epi, int acc_mode, void* out_bf16, float* bgrad, void* workspace,
                    size_t workspace_bytes, fp8ll_stream_t stream);
 
+/* fp8_gemm_dgrad for callers that cannot allocate device memory -- a runtime
+ * whose allocator owns all device memory and forbids allocations after
+ * start-up, a step replayed from a fixed memory plan, or a C caller with no
+ * device allocator.  (The pages have no counterpart: this is a convenience of
+ * this library.)  Same arguments and results as fp8_gemm_dgrad, minus the
+ * workspace: the bias-gradient partials go to a fixed 16 MiB array inside the
+ * library, held by every GPU that loads the library until the process exits.
+ *   - Sizes with fp8_workspace_size(M, N) > 16 MiB (ceil(M/128) * 4 * N > 4 Mi
+ *     partial sums) are refused with FP8LL_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (for
+ *     example on two streams) race on it.  No clearing is needed between
+ *     calls; every partial read is written by the same call first.
+ *   - The call itself allocates nothing and calls no allocating routine. */
+int fp8_gemm_dgrad_noalloc(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                           const void* aux_bf16, int epi, int acc_mode, void* out_bf16, float* bgrad,
+                           fp8ll_stream_t stream);
+
 /* Weight-gradient GEMM ("Weight gradient kernels for dense and MoE models":
  * fp8 x fp8 -> fp32, out += a b^T).
  *   out: fp32 [M][N] contiguous, 16-byte aligned.
