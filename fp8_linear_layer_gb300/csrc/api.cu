@@ -125,11 +125,11 @@ void init_params(GemmParams& p, int64_t M, int64_t N, const fp8ll_operand_t* A, 
     std::memset(&p, 0, sizeof(p));
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
-    p.num_m_tiles = static_cast<int32_t>((M + 127) / 128);
-    p.num_n_tiles = static_cast<int32_t>((N + 255) / 256);
+    p.num_m_tiles = static_cast<int32_t>((M + kTileM - 1) / kTileM);
+    p.num_n_tiles = static_cast<int32_t>((N + kTileN - 1) / kTileN);
     p.tiles_per_group = p.num_m_tiles * p.num_n_tiles;
     p.idesc = (1u << 4) | (static_cast<uint32_t>(A->fmt) << 7) | (static_cast<uint32_t>(B->fmt) << 10) |
-              ((256u >> 3) << 17) | ((128u >> 4) << 24);
+              ((static_cast<uint32_t>(kTileN) >> 3) << 17) | ((static_cast<uint32_t>(kTileM) >> 4) << 24);
     p.status = dev->status;
     const int starve = g_starve_ms.exchange(0);
     if (starve > 0) {
@@ -146,7 +146,7 @@ int grid_for(const GemmParams& p, const DeviceInfo* dev) {
 
 bool valid_mn(int64_t M, int64_t N) {
     if (M < 1 || N < 1 || M > (1LL << 31) - 1 || N > (1LL << 31) - 1) return false;
-    const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+    const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
     return tiles < (1LL << 30) && M * N < (1LL << 46);
 }
 
@@ -208,7 +208,7 @@ int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
     TensorMaps maps;
-    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, 256, &maps.b, &maps.sb))
+    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, kTileN, &maps.b, &maps.sb))
         return FP8LL_ERR_LAUNCH;
     GemmParams p;
     init_params(p, M, N, A, B, dev);
@@ -245,7 +245,7 @@ int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
     TensorMaps maps;
-    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, 256, &maps.b, &maps.sb))
+    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, kTileN, &maps.b, &maps.sb))
         return FP8LL_ERR_LAUNCH;
     GemmParams p;
     init_params(p, M, N, A, B, dev);
@@ -319,7 +319,7 @@ int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const
     if (ng == 0) return FP8LL_OK;
     TensorMaps maps;
     if (!encode_operand(A, M, total_k, 128, &maps.a, &maps.sa) ||
-        !encode_operand(B, N, total_k, 256, &maps.b, &maps.sb))
+        !encode_operand(B, N, total_k, kTileN, &maps.b, &maps.sb))
         return FP8LL_ERR_LAUNCH;
     p.num_groups = ng;
     p.total_tiles = ng * p.tiles_per_group;

@@ -8,29 +8,27 @@
 // epilogues" (bias, tanh-GELU, GELU derivative, bias-gradient column sums) or
 // the fp32 weight-gradient read-modify-write (out += C).
 //
-// CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
-// rasterized tile list:
-//   warp 0      TMA producer: operand tiles (128 x 128 B and 256 x 128 B,
-//               128-byte swizzle) into a 4-stage ring, block scales into an
+// CTA = 4 warpgroups (16 warps), one CTA per SM, persistent over a
+// rasterized tile list of 128 x 192 output tiles:
+//   warp 0      TMA producer: operand tiles (128 x 128 B and 192 x 128 B,
+//               128-byte swizzle) into a 5-stage ring, block scales into an
 //               8-stage ring.
 //   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
-//               (M=128, N=256, K=32, kind::f8f6f4) into one of two TMEM
-//               accumulators (2 x 256 fp32 columns = all 512 columns).
+//               (M=128, N=192, K=32, kind::f8f6f4) into one of two TMEM
+//               accumulators (2 x 192 fp32 columns).
 //   warps 2-3   idle (they complete the first warpgroup).
-//   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4)..+31
-//               (its rows) and one half of the columns; per K block each
-//               thread adds sA*sB*P into a 128-wide fp32 register accumulator
-//               ("promotion"), releasing the TMEM buffer to the MMA warp so
-//               the next block's MMA overlaps this block's promotion.
-// Registers: launched at kLaunchRegs per thread (the most 384 threads can
+//   warps 4-15  promotion + epilogue, three warpgroups of 64 columns each:
+//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block
+//               a thread loads its 64 raw fp32 partial sums with one TMEM load,
+//               hands the buffer straight back to the MMA warp, and then adds
+//               sA*sB*P into a 64-wide fp32 register accumulator
+//               ("promotion") while the next blocks' MMAs run.
+// Registers: launched at kLaunchRegs per thread (the most 512 threads can
 // have), the first warpgroup gives registers back (setmaxnreg.dec to
-// kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
-// kRegsEpi); 128 * kRegsCtrl + 256 * kRegsEpi <= 384 * kLaunchRegs.  The host
+// kRegsCtrl) and the three epilogue warpgroups take them (setmaxnreg.inc to
+// kRegsEpi); 128 * kRegsCtrl + 384 * kRegsEpi <= 512 * kLaunchRegs.  The host
 // refuses to launch if the compiled kernel's register count differs from
 // kLaunchRegs, so the split can never ask for more than the pool.
-// All pipeline waits are bounded (see ptx.cuh); a wait that runs out records
-// a time-out in the status word and every role winds down without touching
-// the outputs further.
 #pragma once
 #include <cstdint>
 
@@ -40,20 +38,23 @@
 
 namespace fp8ll {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBM = kTileM;
+constexpr int kBN = kTileN;
 constexpr int kBK = 128;  // K bytes per stage == one scale block
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kSStages = 8;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiGroups = 3;               // epilogue warpgroups
+constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-constexpr int kLaunchRegs = 168;
+constexpr int kLaunchRegs = 128;
 constexpr int kRegsCtrl = 48;
-constexpr int kRegsEpi = 224;
-static_assert(128 * kRegsCtrl + 256 * kRegsEpi <= kThreads * kLaunchRegs, "register split exceeds the pool");
-constexpr int kHalfN = kBN / 2;
-constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kRegsEpi = 152;
+static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
+              "register split exceeds the pool");
+constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue warp (64)
+static_assert(kHalfN == 64, "one 64-column TMEM load per thread and K block");
+constexpr uint32_t kTmemCols = 512;      // power of two >= 2 * kBN
 constexpr int kRasterM = 16;
 
 struct __align__(1024) SmemLayout {
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         const int ew = warp - kFirstEpiWarp;
         const int q = warp & 3;        // TMEM lane quadrant of this warp
-        const int half = ew >> 2;      // which 128 columns of the tile
+        const int half = ew >> 2;      // which 64 columns of the tile
         const int row = q * 32 + lane; // row within the tile
         int ab = 0, ss = 0;
         uint32_t aph = 0, sph = 0;
@@ -454,15 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        static_cast<uint32_t>(ab * kBN + half * kHalfN);
                 uint32_t r[64];
                 tmem_ld_32x32b_x64_sync(tbase, r);
-                promote_chunk<0>(acc, r, 0, sa2, sbp);
-                promote_chunk<1>(acc, r, 32, sa2, sbp);
-                tmem_ld_32x32b_x64_sync(tbase + 64, r);
-                // every TMEM read of this buffer is complete: hand it back to the MMA warp
+                // the block's partial sums are in registers: hand the buffer back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                promote_chunk<2>(acc, r, 0, sa2, sbp);
-                promote_chunk<3>(acc, r, 32, sa2, sbp);
+                promote_chunk<0>(acc, r, 0, sa2, sbp);
+                promote_chunk<1>(acc, r, 32, sa2, sbp);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
                 ring_advance<2>(ab, aph);
