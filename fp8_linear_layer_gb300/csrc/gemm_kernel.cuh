@@ -8,25 +8,29 @@
 // epilogues" (bias, tanh-GELU, GELU derivative, bias-gradient column sums) or
 // the fp32 weight-gradient read-modify-write (out += C).
 //
-// CTA = 4 warpgroups (16 warps), one CTA per SM, persistent over a
-// rasterized tile list of 128 x 192 output tiles:
-//   warp 0      TMA producer: operand tiles (128 x 128 B and 192 x 128 B,
-//               128-byte swizzle) into a 5-stage ring, block scales into an
-//               8-stage ring.
+// CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
+// rasterized tile list of 128 x 128 output tiles:
+//   warp 0      TMA producer: operand tiles (2 x 128 x 128 B, 128-byte
+//               swizzle) into a 6-stage ring, block scales into an 8-stage
+//               ring.
 //   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
-//               (M=128, N=192, K=32, kind::f8f6f4) into one of two TMEM
-//               accumulators (2 x 192 fp32 columns).
+//               (M=128, N=128, K=32, kind::f8f6f4) into one of four TMEM
+//               accumulators (4 x 128 fp32 columns), so the MMAs can run up to
+//               three blocks ahead of the promotion.
 //   warps 2-3   idle (they complete the first warpgroup).
-//   warps 4-15  promotion + epilogue, three warpgroups of 64 columns each:
-//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block
-//               a thread loads its 64 raw fp32 partial sums with one TMEM load,
-//               hands the buffer straight back to the MMA warp, and then adds
-//               sA*sB*P into a 64-wide fp32 register accumulator
-//               ("promotion") while the next blocks' MMAs run.
-// Registers: launched at kLaunchRegs per thread (the most 512 threads can
+//   warps 4-11  promotion + epilogue, two warpgroups of 64 columns each: warp
+//               w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block a
+//               thread loads its 64 raw fp32 partial sums in two 32-column
+//               halves and adds sA*sB*P into a 64-wide fp32 register
+//               accumulator ("promotion").  The loads are software-pipelined:
+//               the second half is in flight while the first is promoted, and
+//               the next block's first half while the second is promoted, so
+//               the fp32 pipe (which the promotion keeps as busy as the MMAs
+//               keep the tensor pipe) does not idle on TMEM latency.
+// Registers: launched at kLaunchRegs per thread (the most 384 threads can
 // have), the first warpgroup gives registers back (setmaxnreg.dec to
-// kRegsCtrl) and the three epilogue warpgroups take them (setmaxnreg.inc to
-// kRegsEpi); 128 * kRegsCtrl + 384 * kRegsEpi <= 512 * kLaunchRegs.  The host
+// kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
+// kRegsEpi); 128 * kRegsCtrl + 256 * kRegsEpi <= 384 * kLaunchRegs.  The host
 // refuses to launch if the compiled kernel's register count differs from
 // kLaunchRegs, so the split can never ask for more than the pool.
 #pragma once
@@ -41,20 +45,22 @@ namespace fp8ll {
 constexpr int kBM = kTileM;
 constexpr int kBN = kTileN;
 constexpr int kBK = 128;  // K bytes per stage == one scale block
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kSStages = 8;
-constexpr int kEpiGroups = 3;               // epilogue warpgroups
+constexpr int kEpiGroups = 2;               // epilogue warpgroups
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-constexpr int kLaunchRegs = 128;
+constexpr int kLaunchRegs = 168;
 constexpr int kRegsCtrl = 48;
-constexpr int kRegsEpi = 152;
+constexpr int kRegsEpi = 224;
 static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the pool");
 constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue warp (64)
-static_assert(kHalfN == 64, "one 64-column TMEM load per thread and K block");
-constexpr uint32_t kTmemCols = 512;      // power of two >= 2 * kBN
+static_assert(kHalfN == 64, "two 32-column TMEM loads per thread and K block");
+constexpr int kNumAcc = 4;               // TMEM accumulator buffers
+constexpr uint32_t kTmemCols = 512;      // kNumAcc * kBN, a power of two
+static_assert(kNumAcc * kBN <= 512, "TMEM capacity");
 constexpr int kRasterM = 16;
 
 struct __align__(1024) SmemLayout {
@@ -66,8 +72,8 @@ struct __align__(1024) SmemLayout {
     uint64_t empty[kStages];
     uint64_t sfull[kSStages];
     uint64_t sempty[kSStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t acc_full[kNumAcc];
+    uint64_t acc_empty[kNumAcc];
     uint64_t drain;
     uint32_t tmem_base;
 };
@@ -259,20 +265,20 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
     }
 }
 
-// acc[C*16 .. C*16+15] += P[r0 .. r0+31] * (sA * sB[C*32 .. C*32+31]), two columns per
-// packed fp32x2 multiply / fma (each rounded to nearest, as a scalar mul + fma).
+// acc[C*16 .. C*16+15] += P[0..31] * (sA * sB[C*32 .. C*32+31]), two columns
+// per packed fp32x2 multiply / fma (each rounded to nearest, as a scalar mul +
+// fma would be).
 template <int C>
-__device__ __forceinline__ void promote_chunk(float2 (&acc)[kHalfN / 2], const uint32_t (&r)[64], int r0,
-                                              float2 sa2, const float* sbp) {
+__device__ __forceinline__ void promote32(float2 (&acc)[kHalfN / 2], const uint32_t (&r)[32], float2 sa2,
+                                          const float* sbp) {
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
         const float4 sb4 = *reinterpret_cast<const float4*>(sbp + C * 32 + j);
         const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
         const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
         const int a = (C * 32 + j) / 2;
-        acc[a] = __ffma2_rn(make_float2(__uint_as_float(r[r0 + j]), __uint_as_float(r[r0 + j + 1])), s01, acc[a]);
-        acc[a + 1] =
-            __ffma2_rn(make_float2(__uint_as_float(r[r0 + j + 2]), __uint_as_float(r[r0 + j + 3])), s23, acc[a + 1]);
+        acc[a] = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s01, acc[a]);
+        acc[a + 1] = __ffma2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), s23, acc[a + 1]);
     }
 }
 
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&sm.sfull[s]), 1);
             mbar_init(smem_addr(&sm.sempty[s]), kEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNumAcc; ++b) {
             mbar_init(smem_addr(&sm.acc_full[b]), 1);
             mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
         }
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 ring_advance<kStages>(s, ph);
-                ring_advance<2>(ab, aph);
+                ring_advance<kNumAcc>(ab, aph);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
@@ -443,29 +449,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             float2 acc[kHalfN / 2];
 #pragma unroll
             for (int j = 0; j < kHalfN / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-            for (int kb = 0; kb < ge.nkb; ++kb) {
+            const uint32_t tlane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(half * kHalfN);
+            uint32_t r0[32], r1[32];
+            if (ge.nkb > 0) {
                 ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
                 if (ok) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
-                if (!ok) break;
-                tc_fence_after();
+                if (ok) {
+                    tc_fence_after();
+                    tmem_ld_32x32b_x32(tlane + ab * kBN, r0);
+                }
+            }
+            for (int kb = 0; kb < ge.nkb && ok; ++kb) {
                 const float sa = sm.sa[ss][row];
                 const float2 sa2 = make_float2(sa, sa);
                 const float* sbp = &sm.sb[ss][half * kHalfN];
-                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(ab * kBN + half * kHalfN);
-                uint32_t r[64];
-                tmem_ld_32x32b_x64_sync(tbase, r);
-                // the block's partial sums are in registers: hand the buffer back
+                tmem_ld_wait(r0);
+                tmem_ld_32x32b_x32(tlane + ab * kBN + 32, r1);
+                promote32<0>(acc, r0, sa2, sbp);
+                tmem_ld_wait(r1);
+                // both halves of this block are in registers: hand the buffer back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                promote_chunk<0>(acc, r, 0, sa2, sbp);
-                promote_chunk<1>(acc, r, 32, sa2, sbp);
+                ring_advance<kNumAcc>(ab, aph);
+                if (kb + 1 < ge.nkb) {
+                    ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_ld_32x32b_x32(tlane + ab * kBN, r0);  // next block, first half
+                    }
+                }
+                promote32<1>(acc, r1, sa2, sbp);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
-                ring_advance<2>(ab, aph);
                 ring_advance<kSStages>(ss, sph);
+                if (ok && kb + 1 < ge.nkb) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
             }
+            tmem_ld_wait();  // no TMEM load may still be in flight past this point
             if (!ok) break;
             const int r = m0 + row;
             const int cbase = n0 + half * kHalfN;

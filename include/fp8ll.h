@@ -68,8 +68,10 @@ enum {
  * should use fast accumulation": DEFAULT = fast, HIGHEST = full).
  *   FULL: each 128-deep K block's fp32 partial product is promoted into the
  *         fp32 accumulator with its own scale pair as soon as it is ready.
- *   FAST: K blocks are promoted in batches (fewer promotion rounds); each
- *         block still gets its own scale pair. */
+ *   FAST: accepted on every GEMM; with one fp32 scale per row per 128-element
+ *         block, every block's partial product must still meet its own scale
+ *         pair, so FAST currently runs the FULL promotion (same results, same
+ *         speed).  Results meet the FULL bound, inside the FAST one. */
 enum { FP8LL_ACC_FULL = 0, FP8LL_ACC_FAST = 1 };
 
 enum {
