@@ -59,6 +59,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device=None):
+    """The slowest rank's number (all ranks get it); the value itself at N = 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tflops(world, flops_per_step, steps, ms):
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return world * flops_per_step * steps / (ms / 1e3) / 1e12
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -234,15 +250,10 @@ def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
         h_db.copy_(step.db, non_blocking=True)
     ev1.record(stream)
     ev1.synchronize()
-    e2e_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hb, hdY))
     d2h = h_dW.numel() * 4 + h_db.numel() * 4
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_value = tflops(world, flops_step, e2e_steps, e2e_ms)
     return {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": e2e_steps}
 
@@ -308,19 +319,14 @@ def run_ours(args):
     end.synchronize()
     clk = clocks.stop()
     barrier()
-    ms = start.elapsed_time(end)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
     gemm_ms = [a.elapsed_time(b_) for a, b_ in gemm_ev]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     status = fp8.device_status()
     if status != 0:
         raise RuntimeError("device status %d after the timed region" % status)
 
     flops_step = step.gemm_flops
-    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    value = tflops(world, flops_step, args.steps, ms)
     fp8_peak, hbm_peak, peak_src = peaks()
     per_gemm_flops = 2 * m * n * k
     avg_gemm_ms = sum(gemm_ms) / len(gemm_ms)

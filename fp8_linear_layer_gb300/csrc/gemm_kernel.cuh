@@ -8,29 +8,25 @@
 // epilogues" (bias, tanh-GELU, GELU derivative, bias-gradient column sums) or
 // the fp32 weight-gradient read-modify-write (out += C).
 //
-// CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
-// rasterized tile list of 128 x 128 output tiles:
-//   warp 0      TMA producer: operand tiles (2 x 128 x 128 B, 128-byte
-//               swizzle) into a 6-stage ring, block scales into an 8-stage
-//               ring.
+// CTA = 4 warpgroups (16 warps), one CTA per SM, persistent over a
+// rasterized tile list of 128 x 192 output tiles:
+//   warp 0      TMA producer: operand tiles (128 x 128 B and 192 x 128 B,
+//               128-byte swizzle) into a 5-stage ring, block scales into an
+//               8-stage ring.
 //   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
-//               (M=128, N=128, K=32, kind::f8f6f4) into one of four TMEM
-//               accumulators (4 x 128 fp32 columns), so the MMAs can run up to
-//               three blocks ahead of the promotion.
+//               (M=128, N=192, K=32, kind::f8f6f4) into one of two TMEM
+//               accumulators (2 x 192 fp32 columns).
 //   warps 2-3   idle (they complete the first warpgroup).
-//   warps 4-11  promotion + epilogue, two warpgroups of 64 columns each: warp
-//               w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block a
-//               thread loads its 64 raw fp32 partial sums in two 32-column
-//               halves and adds sA*sB*P into a 64-wide fp32 register
-//               accumulator ("promotion").  The loads are software-pipelined:
-//               the second half is in flight while the first is promoted, and
-//               the next block's first half while the second is promoted, so
-//               the fp32 pipe (which the promotion keeps as busy as the MMAs
-//               keep the tensor pipe) does not idle on TMEM latency.
-// Registers: launched at kLaunchRegs per thread (the most 384 threads can
+//   warps 4-15  promotion + epilogue, three warpgroups of 64 columns each:
+//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block
+//               a thread loads its 64 raw fp32 partial sums with one TMEM load,
+//               hands the buffer straight back to the MMA warp, and then adds
+//               sA*sB*P into a 64-wide fp32 register accumulator
+//               ("promotion") while the next blocks' MMAs run.
+// Registers: launched at kLaunchRegs per thread (the most 512 threads can
 // have), the first warpgroup gives registers back (setmaxnreg.dec to
-// kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
-// kRegsEpi); 128 * kRegsCtrl + 256 * kRegsEpi <= 384 * kLaunchRegs.  The host
+// kRegsCtrl) and the three epilogue warpgroups take them (setmaxnreg.inc to
+// kRegsEpi); 128 * kRegsCtrl + 384 * kRegsEpi <= 512 * kLaunchRegs.  The host
 // refuses to launch if the compiled kernel's register count differs from
 // kLaunchRegs, so the split can never ask for more than the pool.
 #pragma once
@@ -45,22 +41,20 @@ namespace fp8ll {
 constexpr int kBM = kTileM;
 constexpr int kBN = kTileN;
 constexpr int kBK = 128;  // K bytes per stage == one scale block
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kSStages = 8;
-constexpr int kEpiGroups = 2;               // epilogue warpgroups
+constexpr int kEpiGroups = 3;               // epilogue warpgroups
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-constexpr int kLaunchRegs = 168;
-constexpr int kRegsCtrl = 48;
-constexpr int kRegsEpi = 224;
+constexpr int kLaunchRegs = 128;
+constexpr int kRegsCtrl = 32;
+constexpr int kRegsEpi = 160;
 static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the pool");
 constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue warp (64)
-static_assert(kHalfN == 64, "two 32-column TMEM loads per thread and K block");
-constexpr int kNumAcc = 4;               // TMEM accumulator buffers
-constexpr uint32_t kTmemCols = 512;      // kNumAcc * kBN, a power of two
-static_assert(kNumAcc * kBN <= 512, "TMEM capacity");
+static_assert(kHalfN == 64, "one 64-column TMEM load per thread and K block");
+constexpr uint32_t kTmemCols = 512;      // power of two >= 2 * kBN
 constexpr int kRasterM = 16;
 
 struct __align__(1024) SmemLayout {
@@ -72,8 +66,8 @@ struct __align__(1024) SmemLayout {
     uint64_t empty[kStages];
     uint64_t sfull[kSStages];
     uint64_t sempty[kSStages];
-    uint64_t acc_full[kNumAcc];
-    uint64_t acc_empty[kNumAcc];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
 };
@@ -265,20 +259,15 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
     }
 }
 
-// acc[C*16 .. C*16+15] += P[0..31] * (sA * sB[C*32 .. C*32+31]), two columns
-// per packed fp32x2 multiply / fma (each rounded to nearest, as a scalar mul +
-// fma would be).
-template <int C>
-__device__ __forceinline__ void promote32(float2 (&acc)[kHalfN / 2], const uint32_t (&r)[32], float2 sa2,
+// acc[i] += P[i] * (sA * sB[2i, 2i+1]) for the 64 columns of this thread, as
+// packed fp32x2 multiplies and fmas (two columns per instruction).
+__device__ __forceinline__ void promote64(uint64_t (&acc)[kHalfN / 2], const uint64_t (&p)[32], uint64_t sa2,
                                           const float* sbp) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        const float4 sb4 = *reinterpret_cast<const float4*>(sbp + C * 32 + j);
-        const float2 s01 = __fmul2_rn(sa2, make_float2(sb4.x, sb4.y));
-        const float2 s23 = __fmul2_rn(sa2, make_float2(sb4.z, sb4.w));
-        const int a = (C * 32 + j) / 2;
-        acc[a] = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s01, acc[a]);
-        acc[a + 1] = __ffma2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), s23, acc[a + 1]);
+    for (int j = 0; j < 16; ++j) {
+        const ulonglong2 sb = *reinterpret_cast<const ulonglong2*>(sbp + 4 * j);
+        acc[2 * j] = fma_f32x2(p[2 * j], mul_f32x2(sa2, sb.x), acc[2 * j]);
+        acc[2 * j + 1] = fma_f32x2(p[2 * j + 1], mul_f32x2(sa2, sb.y), acc[2 * j + 1]);
     }
 }
 
@@ -303,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&sm.sfull[s]), 1);
             mbar_init(smem_addr(&sm.sempty[s]), kEpiWarps);
         }
-        for (int b = 0; b < kNumAcc; ++b) {
+        for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&sm.acc_full[b]), 1);
             mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
         }
@@ -422,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 ring_advance<kStages>(s, ph);
-                ring_advance<kNumAcc>(ab, aph);
+                ring_advance<2>(ab, aph);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
@@ -446,59 +435,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_tile(p, t, g, mt, nt);
             const GroupEntry ge = p.groups[g];
             const int m0 = mt * kBM, n0 = nt * kBN;
-            float2 acc[kHalfN / 2];
+            uint64_t acc[kHalfN / 2];  // packed fp32 pairs: columns 2i, 2i+1
 #pragma unroll
-            for (int j = 0; j < kHalfN / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-            const uint32_t tlane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(half * kHalfN);
-            uint32_t r0[32], r1[32];
-            if (ge.nkb > 0) {
-                ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
-                if (ok) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
-                if (ok) {
-                    tc_fence_after();
-                    tmem_ld_32x32b_x32(tlane + ab * kBN, r0);
-                }
-            }
-            for (int kb = 0; kb < ge.nkb && ok; ++kb) {
+            for (int j = 0; j < kHalfN / 2; ++j) acc[j] = 0ull;
+            for (int kb = 0; kb < ge.nkb; ++kb) {
+                ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
+                if (!ok) break;
+                tc_fence_after();
                 const float sa = sm.sa[ss][row];
-                const float2 sa2 = make_float2(sa, sa);
+                const uint64_t sa2 = pack_f32x2(sa, sa);
                 const float* sbp = &sm.sb[ss][half * kHalfN];
-                tmem_ld_wait(r0);
-                tmem_ld_32x32b_x32(tlane + ab * kBN + 32, r1);
-                promote32<0>(acc, r0, sa2, sbp);
-                tmem_ld_wait(r1);
-                // both halves of this block are in registers: hand the buffer back
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(ab * kBN + half * kHalfN);
+                uint64_t pr[32];
+                tmem_ld_32x32b_x64_pairs(tbase, pr);
+                // the block's partial sums are in registers: hand the buffer back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                ring_advance<kNumAcc>(ab, aph);
-                if (kb + 1 < ge.nkb) {
-                    ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
-                    if (ok) {
-                        tc_fence_after();
-                        tmem_ld_32x32b_x32(tlane + ab * kBN, r0);  // next block, first half
-                    }
-                }
-                promote32<1>(acc, r1, sa2, sbp);
+                promote64(acc, pr, sa2, sbp);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
+                ring_advance<2>(ab, aph);
                 ring_advance<kSStages>(ss, sph);
-                if (ok && kb + 1 < ge.nkb) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
             }
-            tmem_ld_wait();  // no TMEM load may still be in flight past this point
             if (!ok) break;
+            float2 accf[kHalfN / 2];
+#pragma unroll
+            for (int j = 0; j < kHalfN / 2; ++j) accf[j] = unpack_f32x2(acc[j]);
             const int r = m0 + row;
             const int cbase = n0 + half * kHalfN;
             if (EPI == kEpiWgrad) {
-                store_wgrad(p, ge.out_index, r, cbase, acc);
+                store_wgrad(p, ge.out_index, r, cbase, accf);
             } else if (EPI == kEpiNone || EPI == kEpiBias || EPI == kEpiBiasGelu) {
-                store_fprop<EPI>(p, r, cbase, acc);
+                store_fprop<EPI>(p, r, cbase, accf);
             } else {
                 // bias-gradient partials of this warp's 32 rows -> workspace band (4*mt + q)
                 float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
                                                       : nullptr;
-                store_dgrad<EPI == kEpiDgeluBgrad>(p, r, cbase, acc, band, lane);
+                store_dgrad<EPI == kEpiDgeluBgrad>(p, r, cbase, accf, band, lane);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);

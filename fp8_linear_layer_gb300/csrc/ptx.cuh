@@ -52,6 +52,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// One poll of two barriers in one statement (the two latencies overlap).
+__device__ __forceinline__ void mbar_try_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, bool& ok1,
+                                               bool& ok2) {
+    uint32_t r1, r2;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%2], %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q2, [%4], %5;\n\t"
+        "selp.u32 %0, 1, 0, q1;\n\t"
+        "selp.u32 %1, 1, 0, q2;\n\t}"
+        : "=r"(r1), "=r"(r2)
+        : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+        : "memory");
+    ok1 = r1 != 0;
+    ok2 = r2 != 0;
+}
+
 // Wait until the phase with the given parity has completed, for at most
 // budget_ns of wall-clock time.  Returns false on time-out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
@@ -63,6 +80,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
             if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > budget_ns) return false;
     }
+}
+
+// Wait for two phases (each bounded as mbar_wait); both polled at once first.
+__device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, uint64_t budget_ns) {
+    bool ok1, ok2;
+    mbar_try_wait2(b1, p1, b2, p2, ok1, ok2);
+    if (!ok1) ok1 = mbar_wait(b1, p1, budget_ns);
+    if (ok1 && !ok2) ok2 = mbar_wait(b2, p2, budget_ns);
+    return ok1 && ok2;
 }
 
 // ---------------------------------------------------------------------- TMA
@@ -137,18 +163,46 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64_sync(uint32_t taddr, uint32_t
         : "memory");
 }
 
-// Asynchronous form: 32 lanes x 32 consecutive columns into r, completed by a
-// later tmem_ld_wait(r).  Between the two, nothing may read or write r; the
-// wait takes r as in/out operands so every later use depends on it.
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]) : "r"(taddr) : "memory");
+// 32 lanes x 64 consecutive 32-bit columns, returned as 32 packed pairs
+// (column 2i in the low half of p[i]).  Load, completion wait and packing are
+// one asm statement: the destination registers are only defined once the data
+// has arrived, and the pairs come out of the load's consecutive registers.
+__device__ __forceinline__ void tmem_ld_32x32b_x64_pairs(uint32_t taddr, uint64_t (&p)[32]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<64>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31, t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\tmov.b64 %16, {t32, t33};\n\tmov.b64 %17, {t34, t35};\n\tmov.b64 %18, {t36, t37};\n\tmov.b64 %19, {t38, t39};\n\tmov.b64 %20, {t40, t41};\n\tmov.b64 %21, {t42, t43};\n\tmov.b64 %22, {t44, t45};\n\tmov.b64 %23, {t46, t47};\n\tmov.b64 %24, {t48, t49};\n\tmov.b64 %25, {t50, t51};\n\tmov.b64 %26, {t52, t53};\n\tmov.b64 %27, {t54, t55};\n\tmov.b64 %28, {t56, t57};\n\tmov.b64 %29, {t58, t59};\n\tmov.b64 %30, {t60, t61};\n\tmov.b64 %31, {t62, t63};\n\t}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
+        : "r"(taddr)
+        : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) : : "memory");
+// packed fp32x2 arithmetic on 64-bit register pairs (low half = first element);
+// each lane rounds to nearest exactly as the scalar mul / fma would
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row groups 1024 bytes apart.
