@@ -49,6 +49,10 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
+    ap.add_argument("--study", choices=["long_k"], default=None,
+                    help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
+                         "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
+    ap.add_argument("--study-k", type=int, default=16384)
     return ap.parse_args()
 
 
@@ -368,8 +372,77 @@ def run_ours(args):
     return 0
 
 
+def run_long_k_study(args):
+    """Long-K accumulation study: Y = X W^T (bf16 out, no epilogue) with
+    M = N = 16384, K = --study-k; X, W ~ N(0,1) with a seeded 1% of rows of each
+    scaled by 64; e4m3 1x128 casts.  Both accumulation modes are timed (CUDA
+    events) and compared with the oracle on sampled 256 x 256 output tiles
+    (6 random, 2 through outlier rows, the last corner): the reported error is
+    max |gpu - oracle| / sum_k |a b| over those tiles."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    import fp8_linear_layer_gb300 as fp8
+    M = N = 16384
+    K = args.study_k
+    seed = 5000 + K // 1024
+    x, xo = workloads.with_outlier_rows(workloads.normal_bf16((M, K), seed, "X"), seed, "X")
+    w, wo = workloads.with_outlier_rows(workloads.normal_bf16((N, K), seed, "W"), seed, "W")
+    X = fp8.quantize(x.cuda(), fp8.E4M3)
+    W = fp8.quantize(w.cuda(), fp8.E4M3)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    rng = np.random.default_rng(seed)
+    tiles = [(int(rng.integers(0, M // 256)), int(rng.integers(0, N // 256))) for _ in range(6)]
+    tiles += [(int(xo[0]) // 256, int(rng.integers(0, N // 256))), (int(rng.integers(0, M // 256)), int(wo[0]) // 256)]
+    tiles += [(M // 256 - 1, N // 256 - 1)]
+    # oracle: only the rows of X and W the tiles touch
+    rows = sorted({256 * t[0] + i for t in tiles for i in range(256)})
+    cols = sorted({256 * t[1] + i for t in tiles for i in range(256)})
+    rpos = {r: i for i, r in enumerate(rows)}
+    cpos = {c: i for i, c in enumerate(cols)}
+    qa, sa = oracle.quantize(workloads.bits(x[torch.tensor(rows)]), oracle.E4M3)
+    qb, sb = oracle.quantize(workloads.bits(w[torch.tensor(cols)]), oracle.E4M3)
+    t0 = time.perf_counter()
+    ref = []
+    for (ti, tj) in tiles:
+        ri = np.array([rpos[256 * ti + i] for i in range(256)])
+        ci = np.array([cpos[256 * tj + i] for i in range(256)])
+        ref.append(oracle.gemm(qa, sa, oracle.E4M3, qb, sb, oracle.E4M3, rows=ri, cols=ci))
+    oracle_s = time.perf_counter() - t0
+    out = {}
+    for name, mode in (("full", fp8.ACC_FULL), ("fast", fp8.ACC_FAST)):
+        for _ in range(2):
+            fp8.gemm_fprop(X, W, None, fp8.EPI_NONE, mode, out=Y)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        s.record()
+        for _ in range(reps):
+            fp8.gemm_fprop(X, W, None, fp8.EPI_NONE, mode, out=Y)
+        e.record()
+        e.synchronize()
+        ms = s.elapsed_time(e) / reps
+        err = 0.0
+        for (ti, tj), (acc, S) in zip(tiles, ref):
+            got = Y[256 * ti:256 * ti + 256, 256 * tj:256 * tj + 256].float().cpu().double().numpy()
+            err = max(err, float(np.max(np.abs(got - acc) / S)))
+        out[name] = {"tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12, "ms": ms, "max_norm_err": err}
+    if fp8.device_status() != 0:
+        raise RuntimeError("device status not ok")
+    line = {"study": "long_k_accumulation", "M": M, "N": N, "K": K, "outlier_rows": "1% of X and W rows x64",
+            "tiles": "9 of 256x256 (6 random, 2 through outlier rows, last corner)",
+            "note": "max_norm_err includes the bf16 rounding of Y (up to 2^-9 |y| / S)",
+            "bound": {"full": 2e-3, "fast": 8e-3}, "full": out["full"], "fast": out["fast"],
+            "oracle_seconds": round(oracle_s, 1), "oracle_cores": oracle.num_threads()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.study == "long_k":
+        return run_long_k_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -259,18 +259,6 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
     }
 }
 
-// acc[i] += P[i] * (sA * sB[2i, 2i+1]) for the 64 columns of this thread, as
-// packed fp32x2 multiplies and fmas (two columns per instruction).
-__device__ __forceinline__ void promote64(uint64_t (&acc)[kHalfN / 2], const uint64_t (&p)[32], uint64_t sa2,
-                                          const float* sbp) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const ulonglong2 sb = *reinterpret_cast<const ulonglong2*>(sbp + 4 * j);
-        acc[2 * j] = fma_f32x2(p[2 * j], mul_f32x2(sa2, sb.x), acc[2 * j]);
-        acc[2 * j + 1] = fma_f32x2(p[2 * j + 1], mul_f32x2(sa2, sb.y), acc[2 * j + 1]);
-    }
-}
-
 // -------------------------------------------------------------------- kernel
 
 template <int EPI, bool FAST>
@@ -438,26 +426,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t acc[kHalfN / 2];  // packed fp32 pairs: columns 2i, 2i+1
 #pragma unroll
             for (int j = 0; j < kHalfN / 2; ++j) acc[j] = 0ull;
-            for (int kb = 0; kb < ge.nkb; ++kb) {
+            const uint32_t tlane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(half * kHalfN);
+            // Each block is promoted in two 32-column halves; every half's math
+            // runs while the next half's TMEM load is in flight (both inside one
+            // asm statement), so TMEM latency overlaps the fp32 work.
+            uint64_t lo[16], hi[16];
+            if (ge.nkb > 0) {
                 ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
-                if (!ok) break;
-                tc_fence_after();
+                if (ok) {
+                    tc_fence_after();
+                    tmem_ld_32x32b_x32_pairs(tlane + ab * kBN, lo);
+                }
+            }
+            for (int kb = 0; kb < ge.nkb && ok; ++kb) {
                 const float sa = sm.sa[ss][row];
                 const uint64_t sa2 = pack_f32x2(sa, sa);
-                const float* sbp = &sm.sb[ss][half * kHalfN];
-                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(ab * kBN + half * kHalfN);
-                uint64_t pr[32];
-                tmem_ld_32x32b_x64_pairs(tbase, pr);
-                // the block's partial sums are in registers: hand the buffer back
+                const uint32_t sbs = smem_addr(&sm.sb[ss][half * kHalfN]);
+                // promote columns 0-31 while columns 32-63 of this block load
+                promote32_and_load<0>(acc, lo, hi, tlane + ab * kBN + 32, sbs, sa2);
+                // both halves of this block are in registers: hand the buffer back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                promote64(acc, pr, sa2, sbp);
+                ring_advance<2>(ab, aph);
+                const bool more = kb + 1 < ge.nkb;
+                if (more) ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
+                if (more && ok) {
+                    tc_fence_after();
+                    // promote columns 32-63 while columns 0-31 of the next block load
+                    promote32_and_load<1>(acc, hi, lo, tlane + ab * kBN, sbs + 32 * 4, sa2);
+                } else {
+                    promote32<1>(acc, hi, sbs + 32 * 4, sa2);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
-                ring_advance<2>(ab, aph);
                 ring_advance<kSStages>(ss, sph);
+                if (more && ok) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
             }
             if (!ok) break;
             float2 accf[kHalfN / 2];
