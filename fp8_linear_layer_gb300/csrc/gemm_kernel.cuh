@@ -8,25 +8,28 @@
 // epilogues" (bias, tanh-GELU, GELU derivative, bias-gradient column sums) or
 // the fp32 weight-gradient read-modify-write (out += C).
 //
-// CTA = 4 warpgroups (16 warps), one CTA per SM, persistent over a
-// rasterized tile list of 128 x 192 output tiles:
-//   warp 0      TMA producer: operand tiles (128 x 128 B and 192 x 128 B,
-//               128-byte swizzle) into a 5-stage ring, block scales into an
-//               8-stage ring.
+// CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
+// rasterized tile list of 128 x 128 output tiles:
+//   warp 0      TMA producer: operand tiles (2 x 128 x 128 B, 128-byte
+//               swizzle) into a 6-stage ring, block scales into an 8-stage
+//               ring.
 //   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
-//               (M=128, N=192, K=32, kind::f8f6f4) into one of two TMEM
-//               accumulators (2 x 192 fp32 columns).
+//               (M=128, N=128, K=32, kind::f8f6f4) into one of four TMEM
+//               accumulators (4 x 128 fp32 columns), so the MMAs run up to
+//               three blocks ahead of the promotion and the promotion warps
+//               rarely wait for them (they drift out of phase, and one warp's
+//               TMEM load overlaps another's arithmetic).
 //   warps 2-3   idle (they complete the first warpgroup).
-//   warps 4-15  promotion + epilogue, three warpgroups of 64 columns each:
-//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block
-//               a thread loads its 64 raw fp32 partial sums with one TMEM load,
-//               hands the buffer straight back to the MMA warp, and then adds
-//               sA*sB*P into a 64-wide fp32 register accumulator
-//               ("promotion") while the next blocks' MMAs run.
-// Registers: launched at kLaunchRegs per thread (the most 512 threads can
+//   warps 4-11  promotion + epilogue, two warpgroups of 64 columns each: warp
+//               w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block a
+//               thread loads its 64 raw fp32 partial sums with one TMEM load,
+//               hands the buffer straight back to the MMA warp and adds
+//               sA*sB*P into a 64-wide fp32 register accumulator ("promotion")
+//               with packed fp32x2 multiplies and fmas.
+// Registers: launched at kLaunchRegs per thread (the most 384 threads can
 // have), the first warpgroup gives registers back (setmaxnreg.dec to
-// kRegsCtrl) and the three epilogue warpgroups take them (setmaxnreg.inc to
-// kRegsEpi); 128 * kRegsCtrl + 384 * kRegsEpi <= 512 * kLaunchRegs.  The host
+// kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
+// kRegsEpi); 128 * kRegsCtrl + 256 * kRegsEpi <= 384 * kLaunchRegs.  The host
 // refuses to launch if the compiled kernel's register count differs from
 // kLaunchRegs, so the split can never ask for more than the pool.
 #pragma once
@@ -41,20 +44,22 @@ namespace fp8ll {
 constexpr int kBM = kTileM;
 constexpr int kBN = kTileN;
 constexpr int kBK = 128;  // K bytes per stage == one scale block
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kSStages = 8;
-constexpr int kEpiGroups = 3;               // epilogue warpgroups
+constexpr int kEpiGroups = 2;               // epilogue warpgroups
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
-constexpr int kLaunchRegs = 128;
-constexpr int kRegsCtrl = 32;
-constexpr int kRegsEpi = 160;
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtrl = 48;
+constexpr int kRegsEpi = 224;
 static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the pool");
 constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue warp (64)
 static_assert(kHalfN == 64, "one 64-column TMEM load per thread and K block");
-constexpr uint32_t kTmemCols = 512;      // power of two >= 2 * kBN
+constexpr int kNumAcc = 4;               // TMEM accumulator buffers
+constexpr uint32_t kTmemCols = 512;      // kNumAcc * kBN, a power of two
+static_assert(kNumAcc * kBN <= 512, "TMEM capacity");
 constexpr int kRasterM = 16;
 
 struct __align__(1024) SmemLayout {
@@ -66,8 +71,8 @@ struct __align__(1024) SmemLayout {
     uint64_t empty[kStages];
     uint64_t sfull[kSStages];
     uint64_t sempty[kSStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t acc_full[kNumAcc];
+    uint64_t acc_empty[kNumAcc];
     uint64_t drain;
     uint32_t tmem_base;
 };
@@ -259,6 +264,19 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
     }
 }
 
+// acc[i] += P[i] * (sA * sB[2i, 2i+1]) for the 64 columns of this thread, as
+// packed fp32x2 multiplies and fmas (two columns per instruction, each rounded
+// to nearest as the scalar multiply and fma would be).
+__device__ __forceinline__ void promote64(uint64_t (&acc)[kHalfN / 2], const uint64_t (&p)[32], uint64_t sa2,
+                                          const float* sbp) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const ulonglong2 sb = *reinterpret_cast<const ulonglong2*>(sbp + 4 * j);
+        acc[2 * j] = fma_f32x2(p[2 * j], mul_f32x2(sa2, sb.x), acc[2 * j]);
+        acc[2 * j + 1] = fma_f32x2(p[2 * j + 1], mul_f32x2(sa2, sb.y), acc[2 * j + 1]);
+    }
+}
+
 // -------------------------------------------------------------------- kernel
 
 template <int EPI, bool FAST>
@@ -280,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&sm.sfull[s]), 1);
             mbar_init(smem_addr(&sm.sempty[s]), kEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNumAcc; ++b) {
             mbar_init(smem_addr(&sm.acc_full[b]), 1);
             mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
         }
@@ -399,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 ring_advance<kStages>(s, ph);
-                ring_advance<2>(ab, aph);
+                ring_advance<kNumAcc>(ab, aph);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
@@ -428,41 +446,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kHalfN / 2; ++j) acc[j] = 0ull;
             const uint32_t tlane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(half * kHalfN);
-            // Each block is promoted in two 32-column halves; every half's math
-            // runs while the next half's TMEM load is in flight (both inside one
-            // asm statement), so TMEM latency overlaps the fp32 work.
-            uint64_t lo[16], hi[16];
-            if (ge.nkb > 0) {
+            for (int kb = 0; kb < ge.nkb; ++kb) {
                 ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
-                if (ok) {
-                    tc_fence_after();
-                    tmem_ld_32x32b_x32_pairs(tlane + ab * kBN, lo);
-                }
-            }
-            for (int kb = 0; kb < ge.nkb && ok; ++kb) {
-                const float sa = sm.sa[ss][row];
-                const uint64_t sa2 = pack_f32x2(sa, sa);
-                const uint32_t sbs = smem_addr(&sm.sb[ss][half * kHalfN]);
-                // promote columns 0-31 while columns 32-63 of this block load
-                promote32_and_load<0>(acc, lo, hi, tlane + ab * kBN + 32, sbs, sa2);
-                // both halves of this block are in registers: hand the buffer back
+                if (!ok) break;
+                tc_fence_after();
+                uint64_t pr[32];
+                tmem_ld_32x32b_x64_pairs(tlane + ab * kBN, pr);
+                // the block's partial sums are in registers: hand the buffer back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                ring_advance<2>(ab, aph);
-                const bool more = kb + 1 < ge.nkb;
-                if (more) ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
-                if (more && ok) {
-                    tc_fence_after();
-                    // promote columns 32-63 while columns 0-31 of the next block load
-                    promote32_and_load<1>(acc, hi, lo, tlane + ab * kBN, sbs + 32 * 4, sa2);
-                } else {
-                    promote32<1>(acc, hi, sbs + 32 * 4, sa2);
-                }
+                const float sa = sm.sa[ss][row];
+                promote64(acc, pr, pack_f32x2(sa, sa), &sm.sb[ss][half * kHalfN]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
+                ring_advance<kNumAcc>(ab, aph);
                 ring_advance<kSStages>(ss, sph);
-                if (more && ok) ok = warp_all(mbar_wait(smem_addr(&sm.sfull[ss]), sph, budget));
             }
             if (!ok) break;
             float2 accf[kHalfN / 2];

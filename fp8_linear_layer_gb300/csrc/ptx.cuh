@@ -178,45 +178,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64_pairs(uint32_t taddr, uint64_
         : "memory");
 }
 
-// 32 lanes x 32 consecutive columns, waited and returned as 16 packed pairs.
-__device__ __forceinline__ void tmem_ld_32x32b_x32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
-    asm volatile(
-        "{\n\t.reg .b32 t<32>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\t}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
-        : "r"(taddr)
-        : "memory");
-}
-
-// One promotion step of 32 columns overlapped with the next TMEM load, all in
-// one asm statement: issue the load of the next 32 columns into registers
-// private to the statement, promote the current 32 columns
-//   acc[C*16 + i] += cur[i] * (sa2 * sB[2i, 2i+1])   (packed fp32x2, RN)
-// with sB read from shared memory at sb_saddr, then wait for the load and
-// return it packed in `next`.  No register of the load in flight is ever
-// visible outside the statement.
-template <int C>
-__device__ __forceinline__ void promote32_and_load(uint64_t (&acc)[32], const uint64_t (&cur)[16],
-                                                   uint64_t (&next)[16], uint32_t taddr, uint32_t sb_saddr,
-                                                   uint64_t sa2) {
-    asm volatile("{\n\t.reg .b32 t<32>;\n\t.reg .b64 s<16>, c<16>;\n\ttcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%48];\n\tld.shared.v2.b64 {s0, s1}, [%49+0];\n\tld.shared.v2.b64 {s2, s3}, [%49+16];\n\tld.shared.v2.b64 {s4, s5}, [%49+32];\n\tld.shared.v2.b64 {s6, s7}, [%49+48];\n\tld.shared.v2.b64 {s8, s9}, [%49+64];\n\tld.shared.v2.b64 {s10, s11}, [%49+80];\n\tld.shared.v2.b64 {s12, s13}, [%49+96];\n\tld.shared.v2.b64 {s14, s15}, [%49+112];\n\tmul.rn.f32x2 c0, %50, s0;\n\tmul.rn.f32x2 c1, %50, s1;\n\tmul.rn.f32x2 c2, %50, s2;\n\tmul.rn.f32x2 c3, %50, s3;\n\tmul.rn.f32x2 c4, %50, s4;\n\tmul.rn.f32x2 c5, %50, s5;\n\tmul.rn.f32x2 c6, %50, s6;\n\tmul.rn.f32x2 c7, %50, s7;\n\tmul.rn.f32x2 c8, %50, s8;\n\tmul.rn.f32x2 c9, %50, s9;\n\tmul.rn.f32x2 c10, %50, s10;\n\tmul.rn.f32x2 c11, %50, s11;\n\tmul.rn.f32x2 c12, %50, s12;\n\tmul.rn.f32x2 c13, %50, s13;\n\tmul.rn.f32x2 c14, %50, s14;\n\tmul.rn.f32x2 c15, %50, s15;\n\tfma.rn.f32x2 %16, %32, c0, %16;\n\tfma.rn.f32x2 %17, %33, c1, %17;\n\tfma.rn.f32x2 %18, %34, c2, %18;\n\tfma.rn.f32x2 %19, %35, c3, %19;\n\tfma.rn.f32x2 %20, %36, c4, %20;\n\tfma.rn.f32x2 %21, %37, c5, %21;\n\tfma.rn.f32x2 %22, %38, c6, %22;\n\tfma.rn.f32x2 %23, %39, c7, %23;\n\tfma.rn.f32x2 %24, %40, c8, %24;\n\tfma.rn.f32x2 %25, %41, c9, %25;\n\tfma.rn.f32x2 %26, %42, c10, %26;\n\tfma.rn.f32x2 %27, %43, c11, %27;\n\tfma.rn.f32x2 %28, %44, c12, %28;\n\tfma.rn.f32x2 %29, %45, c13, %29;\n\tfma.rn.f32x2 %30, %46, c14, %30;\n\tfma.rn.f32x2 %31, %47, c15, %31;\n\ttcgen05.wait::ld.sync.aligned;\n\tmov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\t}"
-                 : "=l"(next[0]), "=l"(next[1]), "=l"(next[2]), "=l"(next[3]), "=l"(next[4]), "=l"(next[5]), "=l"(next[6]), "=l"(next[7]), "=l"(next[8]), "=l"(next[9]), "=l"(next[10]), "=l"(next[11]), "=l"(next[12]), "=l"(next[13]), "=l"(next[14]), "=l"(next[15]), "+l"(acc[C * 16 + 0]), "+l"(acc[C * 16 + 1]), "+l"(acc[C * 16 + 2]), "+l"(acc[C * 16 + 3]), "+l"(acc[C * 16 + 4]), "+l"(acc[C * 16 + 5]), "+l"(acc[C * 16 + 6]), "+l"(acc[C * 16 + 7]), "+l"(acc[C * 16 + 8]), "+l"(acc[C * 16 + 9]), "+l"(acc[C * 16 + 10]), "+l"(acc[C * 16 + 11]), "+l"(acc[C * 16 + 12]), "+l"(acc[C * 16 + 13]), "+l"(acc[C * 16 + 14]), "+l"(acc[C * 16 + 15])
-                 : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "r"(taddr), "r"(sb_saddr), "l"(sa2)
-                 : "memory");
-}
-
-// The same promotion step with no load (the last block of a tile).
-template <int C>
-__device__ __forceinline__ void promote32(uint64_t (&acc)[32], const uint64_t (&cur)[16], uint32_t sb_saddr,
-                                          uint64_t sa2) {
-    asm volatile("{\n\t.reg .b64 s<16>, c<16>;\n\tld.shared.v2.b64 {s0, s1}, [%33+0];\n\tld.shared.v2.b64 {s2, s3}, [%33+16];\n\tld.shared.v2.b64 {s4, s5}, [%33+32];\n\tld.shared.v2.b64 {s6, s7}, [%33+48];\n\tld.shared.v2.b64 {s8, s9}, [%33+64];\n\tld.shared.v2.b64 {s10, s11}, [%33+80];\n\tld.shared.v2.b64 {s12, s13}, [%33+96];\n\tld.shared.v2.b64 {s14, s15}, [%33+112];\n\tmul.rn.f32x2 c0, %34, s0;\n\tmul.rn.f32x2 c1, %34, s1;\n\tmul.rn.f32x2 c2, %34, s2;\n\tmul.rn.f32x2 c3, %34, s3;\n\tmul.rn.f32x2 c4, %34, s4;\n\tmul.rn.f32x2 c5, %34, s5;\n\tmul.rn.f32x2 c6, %34, s6;\n\tmul.rn.f32x2 c7, %34, s7;\n\tmul.rn.f32x2 c8, %34, s8;\n\tmul.rn.f32x2 c9, %34, s9;\n\tmul.rn.f32x2 c10, %34, s10;\n\tmul.rn.f32x2 c11, %34, s11;\n\tmul.rn.f32x2 c12, %34, s12;\n\tmul.rn.f32x2 c13, %34, s13;\n\tmul.rn.f32x2 c14, %34, s14;\n\tmul.rn.f32x2 c15, %34, s15;\n\tfma.rn.f32x2 %0, %16, c0, %0;\n\tfma.rn.f32x2 %1, %17, c1, %1;\n\tfma.rn.f32x2 %2, %18, c2, %2;\n\tfma.rn.f32x2 %3, %19, c3, %3;\n\tfma.rn.f32x2 %4, %20, c4, %4;\n\tfma.rn.f32x2 %5, %21, c5, %5;\n\tfma.rn.f32x2 %6, %22, c6, %6;\n\tfma.rn.f32x2 %7, %23, c7, %7;\n\tfma.rn.f32x2 %8, %24, c8, %8;\n\tfma.rn.f32x2 %9, %25, c9, %9;\n\tfma.rn.f32x2 %10, %26, c10, %10;\n\tfma.rn.f32x2 %11, %27, c11, %11;\n\tfma.rn.f32x2 %12, %28, c12, %12;\n\tfma.rn.f32x2 %13, %29, c13, %13;\n\tfma.rn.f32x2 %14, %30, c14, %14;\n\tfma.rn.f32x2 %15, %31, c15, %15;\n\t}"
-                 : "+l"(acc[C * 16 + 0]), "+l"(acc[C * 16 + 1]), "+l"(acc[C * 16 + 2]), "+l"(acc[C * 16 + 3]), "+l"(acc[C * 16 + 4]), "+l"(acc[C * 16 + 5]), "+l"(acc[C * 16 + 6]), "+l"(acc[C * 16 + 7]), "+l"(acc[C * 16 + 8]), "+l"(acc[C * 16 + 9]), "+l"(acc[C * 16 + 10]), "+l"(acc[C * 16 + 11]), "+l"(acc[C * 16 + 12]), "+l"(acc[C * 16 + 13]), "+l"(acc[C * 16 + 14]), "+l"(acc[C * 16 + 15])
-                 : "l"(cur[0]), "l"(cur[1]), "l"(cur[2]), "l"(cur[3]), "l"(cur[4]), "l"(cur[5]), "l"(cur[6]), "l"(cur[7]), "l"(cur[8]), "l"(cur[9]), "l"(cur[10]), "l"(cur[11]), "l"(cur[12]), "l"(cur[13]), "l"(cur[14]), "l"(cur[15]), "r"(0u), "r"(sb_saddr), "l"(sa2)
-                 : "memory");
-}
-
 // packed fp32x2 arithmetic on 64-bit register pairs (low half = first element);
 // each lane rounds to nearest exactly as the scalar mul / fma would
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
