@@ -458,6 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
                 const float sa = sm.sa[ss][row];
                 promote64(acc, pr, pack_f32x2(sa, sa), &sm.sb[ss][half * kHalfN]);
+                // the scale stage was read with ordinary loads and is refilled by
+                // TMA: order the reads before the release (cross-proxy hazard)
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
                 ring_advance<kNumAcc>(ab, aph);

@@ -91,6 +91,14 @@ __device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2
     return ok1 && ok2;
 }
 
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (TMA) accesses.  A consumer that read a TMA-filled stage
+// with ordinary loads issues it before releasing the stage, so the next TMA
+// fill of that stage cannot overtake the reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
