@@ -9,23 +9,24 @@
 // the fp32 weight-gradient read-modify-write (out += C).
 //
 // CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
-// rasterized tile list of 128 x 128 output tiles:
-//   warp 0      TMA producer: operand tiles (2 x 128 x 128 B, 128-byte
-//               swizzle) into a 6-stage ring, block scales into an 8-stage
-//               ring.
+// rasterized tile list of 128 x 256 output tiles:
+//   warp 0      TMA producer: operand tiles (128 x 128 B of A, 256 x 128 B of
+//               B, 128-byte swizzle) into a 4-stage ring, block scales into
+//               an 8-stage ring.
 //   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
-//               (M=128, N=128, K=32, kind::f8f6f4) into one of four TMEM
-//               accumulators (4 x 128 fp32 columns), so the MMAs run up to
-//               three blocks ahead of the promotion and the promotion warps
-//               rarely wait for them (they drift out of phase, and one warp's
-//               TMEM load overlaps another's arithmetic).
+//               (M=128, N=256, K=32, kind::f8f6f4) into one of two TMEM
+//               accumulators (2 x 256 fp32 columns), so the MMAs of block
+//               k+1 run while block k is promoted.  An N=256 MMA does twice
+//               the work of an N=128 one for the same A operand read, and
+//               the tensor core only reaches its full rate at this width.
 //   warps 2-3   idle (they complete the first warpgroup).
-//   warps 4-11  promotion + epilogue, two warpgroups of 64 columns each: warp
-//               w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K block a
-//               thread loads its 64 raw fp32 partial sums with one TMEM load,
-//               hands the buffer straight back to the MMA warp and adds
-//               sA*sB*P into a 64-wide fp32 register accumulator ("promotion")
-//               with packed fp32x2 multiplies and fmas.
+//   warps 4-11  promotion + epilogue, two warpgroups of 128 columns each:
+//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K
+//               block a thread loads its raw fp32 partial sums in two
+//               64-column TMEM loads, hands the buffer back to the MMA warp
+//               after the second and adds sA*sB*P into a 128-wide fp32
+//               register accumulator ("promotion") with packed fp32x2
+//               multiplies and fmas.
 // Registers: launched at kLaunchRegs per thread (the most 384 threads can
 // have), the first warpgroup gives registers back (setmaxnreg.dec to
 // kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
@@ -44,20 +45,20 @@ namespace fp8ll {
 constexpr int kBM = kTileM;
 constexpr int kBN = kTileN;
 constexpr int kBK = 128;  // K bytes per stage == one scale block
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kSStages = 8;
 constexpr int kEpiGroups = 2;               // epilogue warpgroups
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr int kLaunchRegs = 168;
-constexpr int kRegsCtrl = 48;
-constexpr int kRegsEpi = 224;
+constexpr int kRegsCtrl = 40;
+constexpr int kRegsEpi = 232;
 static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the pool");
-constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue warp (64)
-static_assert(kHalfN == 64, "one 64-column TMEM load per thread and K block");
-constexpr int kNumAcc = 4;               // TMEM accumulator buffers
+constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue thread (128)
+static_assert(kHalfN == 128, "two 64-column TMEM loads per thread and K block");
+constexpr int kNumAcc = 2;               // TMEM accumulator buffers
 constexpr uint32_t kTmemCols = 512;      // kNumAcc * kBN, a power of two
 static_assert(kNumAcc * kBN <= 512, "TMEM capacity");
 constexpr int kRasterM = 16;
@@ -264,13 +265,13 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbas
     }
 }
 
-// acc[i] += P[i] * (sA * sB[2i, 2i+1]) for the 64 columns of this thread, as
+// acc[i] += P[i] * (sA * sB[2i, 2i+1]) for 32 columns of this thread, as
 // packed fp32x2 multiplies and fmas (two columns per instruction, each rounded
-// to nearest as the scalar multiply and fma would be).
-__device__ __forceinline__ void promote64(uint64_t (&acc)[kHalfN / 2], const uint64_t (&p)[32], uint64_t sa2,
-                                          const float* sbp) {
+// to nearest as the scalar multiply and fma would be).  acc points into the
+// thread's register accumulator at a compile-time offset.
+__device__ __forceinline__ void promote32(uint64_t* acc, const uint64_t* p, uint64_t sa2, const float* sbp) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 8; ++j) {
         const ulonglong2 sb = *reinterpret_cast<const ulonglong2*>(sbp + 4 * j);
         acc[2 * j] = fma_f32x2(p[2 * j], mul_f32x2(sa2, sb.x), acc[2 * j]);
         acc[2 * j + 1] = fma_f32x2(p[2 * j + 1], mul_f32x2(sa2, sb.y), acc[2 * j + 1]);
@@ -450,14 +451,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
                 if (!ok) break;
                 tc_fence_after();
-                uint64_t pr[32];
-                tmem_ld_32x32b_x64_pairs(tlane + ab * kBN, pr);
-                // the block's partial sums are in registers: hand the buffer back
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+                const uint32_t tbuf = tlane + ab * kBN;
                 const float sa = sm.sa[ss][row];
-                promote64(acc, pr, pack_f32x2(sa, sa), &sm.sb[ss][half * kHalfN]);
+                const uint64_t sa2 = pack_f32x2(sa, sa);
+                const float* sbp = &sm.sb[ss][half * kHalfN];
+                // two 64-column TMEM loads; the buffer goes back to the MMA warp
+                // as soon as the second one has landed
+                {
+                    uint64_t pr[32];
+                    tmem_ld_32x32b_x64_pairs(tbuf, pr);
+                    promote32(&acc[0], &pr[0], sa2, sbp);
+                    promote32(&acc[16], &pr[16], sa2, sbp + 32);
+                }
+                {
+                    uint64_t pr[32];
+                    tmem_ld_32x32b_x64_pairs(tbuf + 64, pr);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+                    promote32(&acc[32], &pr[0], sa2, sbp + 64);
+                    promote32(&acc[48], &pr[16], sa2, sbp + 96);
+                }
                 // the scale stage was read with ordinary loads and is refilled by
                 // TMA: order the reads before the release (cross-proxy hazard)
                 fence_proxy_async_smem();

@@ -8,7 +8,7 @@ namespace fp8ll {
 
 constexpr int kMaxGroups = 256;
 constexpr int kTileM = 128;  // GEMM output tile rows
-constexpr int kTileN = 128;  // GEMM output tile columns
+constexpr int kTileN = 256;  // GEMM output tile columns
 
 enum EpiKind : int {
     kEpiNone = 0,

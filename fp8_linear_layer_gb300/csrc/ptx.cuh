@@ -186,6 +186,20 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64_pairs(uint32_t taddr, uint64_
         : "memory");
 }
 
+// 32 consecutive columns of this warp's 32 TMEM lanes, returned as 16 packed
+// fp32 pairs; the wait is inside the same statement, so no use of the outputs
+// can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld_32x32b_x32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\t}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // packed fp32x2 arithmetic on 64-bit register pairs (low half = first element);
 // each lane rounds to nearest exactly as the scalar mul / fma would
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
