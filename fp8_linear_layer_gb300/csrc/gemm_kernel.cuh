@@ -21,12 +21,16 @@
 //               the tensor core only reaches its full rate at this width.
 //   warps 2-3   idle (they complete the first warpgroup).
 //   warps 4-11  promotion + epilogue, two warpgroups of 128 columns each:
-//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows).  Per K
-//               block a thread loads its raw fp32 partial sums in two
-//               64-column TMEM loads, hands the buffer back to the MMA warp
-//               after the second and adds sA*sB*P into a 128-wide fp32
-//               register accumulator ("promotion") with packed fp32x2
-//               multiplies and fmas.
+//               warp w reads TMEM lanes 32*(w%4)..+31 (its rows) in the
+//               16x256b fragment shape, so a thread holds four rows x two
+//               columns of every 8-column chunk.  Per K block it loads its raw
+//               fp32 partial sums with two pairs of 16-lane loads, hands the
+//               buffer back to the MMA warp after the second pair and adds
+//               sA*sB*P into a 128-element fp32 register accumulator
+//               ("promotion") with packed fp32x2 multiplies and fmas.  One
+//               8-byte column-scale load serves eight elements: the scale
+//               loads draw on shared-memory bandwidth, which the tensor
+//               core's operand reads need as well.
 // Registers: launched at kLaunchRegs per thread (the most 384 threads can
 // have), the first warpgroup gives registers back (setmaxnreg.dec to
 // kRegsCtrl) and the two epilogue warpgroups take them (setmaxnreg.inc to
@@ -57,7 +61,7 @@ constexpr int kRegsEpi = 232;
 static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the pool");
 constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue thread (128)
-static_assert(kHalfN == 128, "two 64-column TMEM loads per thread and K block");
+static_assert(kHalfN == 128, "two 16x256b.x8 TMEM load pairs per thread and K block");
 constexpr int kNumAcc = 2;               // TMEM accumulator buffers
 constexpr uint32_t kTmemCols = 512;      // kNumAcc * kBN, a power of two
 static_assert(kNumAcc * kBN <= 512, "TMEM capacity");
@@ -107,174 +111,143 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v) != 0; }
 
 // ------------------------------------------------------------------ stores
+//
+// After the promotion a thread holds the 16x256b TMEM fragment of its warp:
+// rows row0 + 8r (r = 0..3) and column pairs col0 + 8c + {0, 1} (c = 0..15),
+// packed as acc[4c + r] (even column in the low half), where
+// row0 = m0 + 32 * quadrant + lane / 4 and col0 = n0 + 128 * half + 2 * (lane % 4).
 
-// wgrad: out (+)= acc, fp32
-// out += acc is a single fp32 add per element, done in L2 by a vector
-// reduction (no load round trip; each element receives exactly one add per
-// call, so the result is deterministic).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+constexpr int kChunks = kHalfN / 8;  // 8-column chunks per thread (16)
+
+__device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
 }
 
-__device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, int r, int cbase,
-                                            float2 (&acc)[kHalfN / 2]) {
-    if (r >= p.M) return;
-    float* orow = static_cast<float*>(p.out) + (static_cast<int64_t>(out_index) * p.M + r) * p.N + cbase;
-    if ((p.N & 3) == 0 && cbase + kHalfN <= p.N) {
-        if (p.accumulate) {
+// wgrad: out (+)= acc, fp32.  out += acc is a single fp32 add per element,
+// done in L2 by a vector reduction (no load round trip; each element receives
+// exactly one add per call, so the result is deterministic).
+__device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, int row0, int col0,
+                                            const uint64_t (&acc)[4 * kChunks]) {
+    const bool pairs = (p.N & 1) == 0;  // column pairs are 8-byte aligned
 #pragma unroll
-            for (int j = 0; j < kHalfN; j += 4)
-                red_add_v4(orow + j, acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
-        } else {
+    for (int r = 0; r < 4; ++r) {
+        const int row = row0 + 8 * r;
+        if (row >= p.M) continue;
+        float* orow = static_cast<float*>(p.out) + (static_cast<int64_t>(out_index) * p.M + row) * p.N;
 #pragma unroll
-            for (int j = 0; j < kHalfN; j += 4)
-                *reinterpret_cast<float4*>(orow + j) =
-                    make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kHalfN; ++j) {
-            const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-            if (cbase + j < p.N) orow[j] = (p.accumulate ? orow[j] : 0.0f) + v;
+        for (int c = 0; c < kChunks; ++c) {
+            const int col = col0 + 8 * c;
+            const float2 v = unpack_f32x2(acc[4 * c + r]);
+            if (pairs) {
+                if (col < p.N) {
+                    if (p.accumulate)
+                        red_add_v2(orow + col, v.x, v.y);
+                    else
+                        *reinterpret_cast<float2*>(orow + col) = v;
+                }
+            } else {
+                if (col < p.N) orow[col] = (p.accumulate ? orow[col] : 0.0f) + v.x;
+                if (col + 1 < p.N) orow[col + 1] = (p.accumulate ? orow[col + 1] : 0.0f) + v.y;
+            }
         }
     }
 }
 
 // fprop: Z = acc + bias[j]; Y = gelu(Z) or Z; bf16 out (+ bf16 aux Z)
 template <int EPI>
-__device__ __forceinline__ void store_fprop(const GemmParams& p, int r, int cbase, float2 (&acc)[kHalfN / 2]) {
-    if (r >= p.M) return;
-    const int64_t off = static_cast<int64_t>(r) * p.N + cbase;
-    uint16_t* out = static_cast<uint16_t*>(p.out) + off;
-    uint16_t* aux = (EPI == kEpiBiasGelu && p.aux) ? static_cast<uint16_t*>(p.aux) + off : nullptr;
-    const uint16_t* bias = static_cast<const uint16_t*>(p.bias) + cbase;
-    if ((p.N & 7) == 0 && cbase + kHalfN <= p.N) {
+__device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int col0,
+                                            const uint64_t (&acc)[4 * kChunks]) {
+    const bool pairs = (p.N & 1) == 0;
+    uint16_t* out = static_cast<uint16_t*>(p.out);
+    uint16_t* aux = (EPI == kEpiBiasGelu) ? static_cast<uint16_t*>(p.aux) : nullptr;
+    const uint16_t* bias = static_cast<const uint16_t*>(p.bias);
 #pragma unroll
-        for (int j = 0; j < kHalfN; j += 8) {
-            float z[8];
-            if (EPI == kEpiNone) {
+    for (int c = 0; c < kChunks; ++c) {
+        const int col = col0 + 8 * c;
+        if (col >= p.N) continue;
+        const bool two = col + 1 < p.N;
+        float b0 = 0.0f, b1 = 0.0f;
+        if (EPI != kEpiNone) {
+            b0 = __uint_as_float(static_cast<uint32_t>(bias[col]) << 16);
+            if (two) b1 = __uint_as_float(static_cast<uint32_t>(bias[col + 1]) << 16);
+        }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    z[2 * i] = acc[j / 2 + i].x;
-                    z[2 * i + 1] = acc[j / 2 + i].y;
-                }
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + 8 * r;
+            if (row >= p.M) continue;
+            const float2 a = unpack_f32x2(acc[4 * c + r]);
+            const float z0 = a.x + b0, z1 = a.y + b1;
+            const float y0 = (EPI == kEpiBiasGelu) ? gelu_tanh(z0) : z0;
+            const float y1 = (EPI == kEpiBiasGelu) ? gelu_tanh(z1) : z1;
+            const int64_t off = static_cast<int64_t>(row) * p.N + col;
+            if (pairs) {
+                *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(y0, y1);
+                if (aux) *reinterpret_cast<uint32_t*>(aux + off) = pack_bf16x2(z0, z1);
             } else {
-                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + j));
-                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    z[2 * i] = acc[j / 2 + i].x + bf16_lo(bw[i]);
-                    z[2 * i + 1] = acc[j / 2 + i].y + bf16_hi(bw[i]);
+                out[off] = static_cast<uint16_t>(pack_bf16x2(y0, 0.0f) & 0xFFFFu);
+                if (aux) aux[off] = static_cast<uint16_t>(pack_bf16x2(z0, 0.0f) & 0xFFFFu);
+                if (two) {
+                    out[off + 1] = static_cast<uint16_t>(pack_bf16x2(y1, 0.0f) & 0xFFFFu);
+                    if (aux) aux[off + 1] = static_cast<uint16_t>(pack_bf16x2(z1, 0.0f) & 0xFFFFu);
                 }
             }
-            uint32_t yw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (EPI == kEpiBiasGelu)
-                    yw[i] = pack_bf16x2(gelu_tanh(z[2 * i]), gelu_tanh(z[2 * i + 1]));
-                else
-                    yw[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
-            }
-            *reinterpret_cast<uint4*>(out + j) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-            if (aux) {
-                *reinterpret_cast<uint4*>(aux + j) =
-                    make_uint4(pack_bf16x2(z[0], z[1]), pack_bf16x2(z[2], z[3]), pack_bf16x2(z[4], z[5]),
-                               pack_bf16x2(z[6], z[7]));
-            }
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kHalfN; ++j) {
-            if (cbase + j < p.N) {
-                float z = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-                if (EPI != kEpiNone) z += __uint_as_float(static_cast<uint32_t>(bias[j]) << 16);
-                const float y = (EPI == kEpiBiasGelu) ? gelu_tanh(z) : z;
-                out[j] = static_cast<uint16_t>(pack_bf16x2(y, 0.0f) & 0xFFFFu);
-                if (aux) aux[j] = static_cast<uint16_t>(pack_bf16x2(z, 0.0f) & 0xFFFFu);
-            }
         }
     }
 }
 
-// Column sums of 32 consecutive columns over the 32 rows held by a warp:
-// a butterfly that halves the column set at each step.  Afterwards lane l
-// holds the sum for column l.  The summation order is fixed, so results are
-// deterministic.
-__device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < off; ++i) {
-            const float send = upper ? v[i] : v[i + off];
-            const float keep = upper ? v[i + off] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
-    return v[0];
-}
-
-// dgrad: dZ = acc * gelu'(Z) -> bf16 out, 32 columns at a time.  With BGRAD,
-// each 32-column chunk's fp32 dZ (zero outside the matrix) is summed over the
-// warp's 32 rows and written to the workspace band of this warp.
+// dgrad: dZ = acc * gelu'(Z) -> bf16 out.  With BGRAD the fp32 dZ of each
+// column (zero outside the matrix) is summed over the warp's 32 rows -- the
+// thread's four rows first, then across the eight lanes that hold the same
+// columns (lane xor 4, 8, 16), a fixed order, so results are deterministic --
+// and lanes 0..3 write the chunk's eight sums to the workspace band of this warp.
 template <bool BGRAD>
-__device__ __forceinline__ void store_dgrad(const GemmParams& p, int r, int cbase, float2 (&acc)[kHalfN / 2],
-                                            float* band, int lane) {
-    const bool row_ok = r < p.M;
-    const int64_t off = static_cast<int64_t>(row_ok ? r : 0) * p.N + cbase;
-    uint16_t* out = static_cast<uint16_t*>(p.out) + off;
-    const uint16_t* zp = static_cast<const uint16_t*>(p.aux) + off;
-    const bool vec = (p.N & 7) == 0 && cbase + kHalfN <= p.N;
+__device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int col0,
+                                            const uint64_t (&acc)[4 * kChunks], float* band, int lane) {
+    const bool pairs = (p.N & 1) == 0;
+    uint16_t* out = static_cast<uint16_t*>(p.out);
+    const uint16_t* zp = static_cast<const uint16_t*>(p.aux);
 #pragma unroll
-    for (int c = 0; c < kHalfN / 32; ++c) {
-        float v[32];
-        if (row_ok && vec) {
+    for (int c = 0; c < kChunks; ++c) {
+        const int col = col0 + 8 * c;
+        const bool one = col < p.N, two = col + 1 < p.N;
+        float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-                const uint4 zv = *reinterpret_cast<const uint4*>(zp + c * 32 + j);
-                const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-                uint32_t ow[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 a = acc[(c * 32 + j) / 2 + i];
-                    v[j + 2 * i] = a.x * dgelu_tanh(bf16_lo(zw[i]));
-                    v[j + 2 * i + 1] = a.y * dgelu_tanh(bf16_hi(zw[i]));
-                    ow[i] = pack_bf16x2(v[j + 2 * i], v[j + 2 * i + 1]);
-                }
-                *reinterpret_cast<uint4*>(out + c * 32 + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + 8 * r;
+            if (row >= p.M || !one) continue;
+            const float2 a = unpack_f32x2(acc[4 * c + r]);
+            const int64_t off = static_cast<int64_t>(row) * p.N + col;
+            float z0, z1 = 0.0f;
+            if (pairs) {
+                const uint32_t zw = *reinterpret_cast<const uint32_t*>(zp + off);
+                z0 = bf16_lo(zw);
+                z1 = bf16_hi(zw);
+            } else {
+                z0 = __uint_as_float(static_cast<uint32_t>(zp[off]) << 16);
+                if (two) z1 = __uint_as_float(static_cast<uint32_t>(zp[off + 1]) << 16);
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int col = cbase + c * 32 + j;
-                const float a = (j & 1) ? acc[(c * 32 + j) / 2].y : acc[(c * 32 + j) / 2].x;
-                v[j] = 0.0f;
-                if (row_ok && col < p.N) {
-                    const float z = __uint_as_float(static_cast<uint32_t>(zp[c * 32 + j]) << 16);
-                    v[j] = a * dgelu_tanh(z);
-                    out[c * 32 + j] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
-                }
+            const float d0 = a.x * dgelu_tanh(z0);
+            const float d1 = two ? a.y * dgelu_tanh(z1) : 0.0f;
+            if (pairs) {
+                *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(d0, d1);
+            } else {
+                out[off] = static_cast<uint16_t>(pack_bf16x2(d0, 0.0f) & 0xFFFFu);
+                if (two) out[off + 1] = static_cast<uint16_t>(pack_bf16x2(d1, 0.0f) & 0xFFFFu);
             }
+            s0 += d0;
+            s1 += d1;
         }
         if (BGRAD) {
-            const float s = warp_column_sum32(v, lane);
-            const int col = cbase + c * 32 + lane;
-            if (col < p.N) band[col] = s;
-        }
-    }
-}
-
-// acc[i] += P[i] * (sA * sB[2i, 2i+1]) for 32 columns of this thread, as
-// packed fp32x2 multiplies and fmas (two columns per instruction, each rounded
-// to nearest as the scalar multiply and fma would be).  acc points into the
-// thread's register accumulator at a compile-time offset.
-__device__ __forceinline__ void promote32(uint64_t* acc, const uint64_t* p, uint64_t sa2, const float* sbp) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const ulonglong2 sb = *reinterpret_cast<const ulonglong2*>(sbp + 4 * j);
-        acc[2 * j] = fma_f32x2(p[2 * j], mul_f32x2(sa2, sb.x), acc[2 * j]);
-        acc[2 * j + 1] = fma_f32x2(p[2 * j + 1], mul_f32x2(sa2, sb.y), acc[2 * j + 1]);
+            for (int m = 4; m <= 16; m <<= 1) {
+                s0 += __shfl_xor_sync(0xffffffffu, s0, m);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, m);
+            }
+            if (lane < 4) {
+                if (one) band[col] = s0;
+                if (two) band[col + 1] = s1;
+            }
+        }
     }
 }
 
@@ -431,9 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------ promotion and epilogue
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         const int ew = warp - kFirstEpiWarp;
-        const int q = warp & 3;        // TMEM lane quadrant of this warp
-        const int half = ew >> 2;      // which 64 columns of the tile
-        const int row = q * 32 + lane; // row within the tile
+        const int q = warp & 3;    // TMEM lane quadrant of this warp
+        const int half = ew >> 2;  // which 128 columns of the tile
+        const int g8 = lane >> 2;  // row within each 8-row group
+        const int cq = lane & 3;   // column pair within each 8-column chunk
         int ab = 0, ss = 0;
         uint32_t aph = 0, sph = 0;
         bool ok = true;
@@ -442,35 +416,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_tile(p, t, g, mt, nt);
             const GroupEntry ge = p.groups[g];
             const int m0 = mt * kBM, n0 = nt * kBN;
-            uint64_t acc[kHalfN / 2];  // packed fp32 pairs: columns 2i, 2i+1
+            uint64_t acc[4 * kChunks];  // packed fp32 pairs, layout described above the stores
 #pragma unroll
-            for (int j = 0; j < kHalfN / 2; ++j) acc[j] = 0ull;
-            const uint32_t tlane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(half * kHalfN);
+            for (int j = 0; j < 4 * kChunks; ++j) acc[j] = 0ull;
+            const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(half * kHalfN);
             for (int kb = 0; kb < ge.nkb; ++kb) {
                 ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tbuf = tlane + ab * kBN;
-                const float sa = sm.sa[ss][row];
-                const uint64_t sa2 = pack_f32x2(sa, sa);
-                const float* sbp = &sm.sb[ss][half * kHalfN];
-                // two 64-column TMEM loads; the buffer goes back to the MMA warp
-                // as soon as the second one has landed
-                {
-                    uint64_t pr[32];
-                    tmem_ld_32x32b_x64_pairs(tbuf, pr);
-                    promote32(&acc[0], &pr[0], sa2, sbp);
-                    promote32(&acc[16], &pr[16], sa2, sbp + 32);
+                const uint32_t tbuf = tq + static_cast<uint32_t>(ab * kBN);
+                // row scales of the thread's four rows; column scales one pair per
+                // chunk, shared by the four rows (one 8-byte load per 8 elements)
+                uint64_t sa2[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float s = sm.sa[ss][q * 32 + g8 + 8 * r];
+                    sa2[r] = pack_f32x2(s, s);
                 }
-                {
-                    uint64_t pr[32];
-                    tmem_ld_32x32b_x64_pairs(tbuf + 64, pr);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
-                    promote32(&acc[32], &pr[0], sa2, sbp + 64);
-                    promote32(&acc[48], &pr[16], sa2, sbp + 96);
+                const float* sbp = &sm.sb[ss][half * kHalfN + 2 * cq];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint64_t plo[16], phi[16];
+                    tmem_ld_16x256b_x8_pairs2(tbuf + 64u * h, tbuf + (16u << 16) + 64u * h, plo, phi);
+                    if (h == 1) {
+                        // the block's partial sums are all in registers: hand the buffer back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = 8 * h + i;
+                        const uint64_t sb = *reinterpret_cast<const uint64_t*>(sbp + 8 * c);
+                        acc[4 * c + 0] = fma_f32x2(plo[2 * i], mul_f32x2(sa2[0], sb), acc[4 * c + 0]);
+                        acc[4 * c + 1] = fma_f32x2(plo[2 * i + 1], mul_f32x2(sa2[1], sb), acc[4 * c + 1]);
+                        acc[4 * c + 2] = fma_f32x2(phi[2 * i], mul_f32x2(sa2[2], sb), acc[4 * c + 2]);
+                        acc[4 * c + 3] = fma_f32x2(phi[2 * i + 1], mul_f32x2(sa2[3], sb), acc[4 * c + 3]);
+                    }
                 }
                 // the scale stage was read with ordinary loads and is refilled by
                 // TMA: order the reads before the release (cross-proxy hazard)
@@ -481,20 +464,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ring_advance<kSStages>(ss, sph);
             }
             if (!ok) break;
-            float2 accf[kHalfN / 2];
-#pragma unroll
-            for (int j = 0; j < kHalfN / 2; ++j) accf[j] = unpack_f32x2(acc[j]);
-            const int r = m0 + row;
-            const int cbase = n0 + half * kHalfN;
+            const int row0 = m0 + q * 32 + g8;
+            const int col0 = n0 + half * kHalfN + 2 * cq;
             if (EPI == kEpiWgrad) {
-                store_wgrad(p, ge.out_index, r, cbase, accf);
+                store_wgrad(p, ge.out_index, row0, col0, acc);
             } else if (EPI == kEpiNone || EPI == kEpiBias || EPI == kEpiBiasGelu) {
-                store_fprop<EPI>(p, r, cbase, accf);
+                store_fprop<EPI>(p, row0, col0, acc);
             } else {
                 // bias-gradient partials of this warp's 32 rows -> workspace band (4*mt + q)
                 float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
                                                       : nullptr;
-                store_dgrad<EPI == kEpiDgeluBgrad>(p, r, cbase, accf, band, lane);
+                store_dgrad<EPI == kEpiDgeluBgrad>(p, row0, col0, acc, band, lane);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
