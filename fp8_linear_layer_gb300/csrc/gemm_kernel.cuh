@@ -161,16 +161,26 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int c
     uint16_t* out = static_cast<uint16_t*>(p.out);
     uint16_t* aux = (EPI == kEpiBiasGelu) ? static_cast<uint16_t*>(p.aux) : nullptr;
     const uint16_t* bias = static_cast<const uint16_t*>(p.bias);
+    // the bias pairs of all chunks first, so that their loads are in flight together
+    uint32_t bw[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const int col = col0 + 8 * c;
+        bw[c] = 0u;
+        if (EPI != kEpiNone && col < p.N) {
+            if (pairs)
+                bw[c] = __ldg(reinterpret_cast<const unsigned int*>(bias + col));
+            else
+                bw[c] = static_cast<uint32_t>(bias[col]) |
+                        (col + 1 < p.N ? static_cast<uint32_t>(bias[col + 1]) << 16 : 0u);
+        }
+    }
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int col = col0 + 8 * c;
         if (col >= p.N) continue;
         const bool two = col + 1 < p.N;
-        float b0 = 0.0f, b1 = 0.0f;
-        if (EPI != kEpiNone) {
-            b0 = __uint_as_float(static_cast<uint32_t>(bias[col]) << 16);
-            if (two) b1 = __uint_as_float(static_cast<uint32_t>(bias[col + 1]) << 16);
-        }
+        const float b0 = bf16_lo(bw[c]), b1 = bf16_hi(bw[c]);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int row = row0 + 8 * r;
@@ -206,6 +216,26 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
     const bool pairs = (p.N & 1) == 0;
     uint16_t* out = static_cast<uint16_t*>(p.out);
     const uint16_t* zp = static_cast<const uint16_t*>(p.aux);
+    // all of the thread's stored pre-activations first (bf16 pairs), so that
+    // the loads are in flight together
+    uint32_t zw[4 * kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const int col = col0 + 8 * c;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + 8 * r;
+            zw[4 * c + r] = 0u;
+            if (row < p.M && col < p.N) {
+                const int64_t off = static_cast<int64_t>(row) * p.N + col;
+                if (pairs)
+                    zw[4 * c + r] = *reinterpret_cast<const uint32_t*>(zp + off);
+                else
+                    zw[4 * c + r] = static_cast<uint32_t>(zp[off]) |
+                                    (col + 1 < p.N ? static_cast<uint32_t>(zp[off + 1]) << 16 : 0u);
+            }
+        }
+    }
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int col = col0 + 8 * c;
@@ -217,15 +247,7 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
             if (row >= p.M || !one) continue;
             const float2 a = unpack_f32x2(acc[4 * c + r]);
             const int64_t off = static_cast<int64_t>(row) * p.N + col;
-            float z0, z1 = 0.0f;
-            if (pairs) {
-                const uint32_t zw = *reinterpret_cast<const uint32_t*>(zp + off);
-                z0 = bf16_lo(zw);
-                z1 = bf16_hi(zw);
-            } else {
-                z0 = __uint_as_float(static_cast<uint32_t>(zp[off]) << 16);
-                if (two) z1 = __uint_as_float(static_cast<uint32_t>(zp[off + 1]) << 16);
-            }
+            const float z0 = bf16_lo(zw[4 * c + r]), z1 = bf16_hi(zw[4 * c + r]);
             const float d0 = a.x * dgelu_tanh(z0);
             const float d1 = two ? a.y * dgelu_tanh(z1) : 0.0f;
             if (pairs) {
@@ -421,6 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4 * kChunks; ++j) acc[j] = 0ull;
             const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(half * kHalfN);
+            if (EPI == kEpiDgelu || EPI == kEpiDgeluBgrad) {
+                // the stored pre-activations of this tile are read once the K loop
+                // is done: ask for them in L2 now (each lane of a quad one of the
+                // quad's four rows; a row's 128 columns span at most three lines)
+                const int prow = m0 + q * 32 + g8 + 8 * cq;
+                const int pc0 = n0 + half * kHalfN;
+                if (prow < p.M && pc0 < p.N) {
+                    const uint16_t* zrow = static_cast<const uint16_t*>(p.aux) + static_cast<int64_t>(prow) * p.N;
+                    const int pc1 = min(pc0 + kHalfN - 1, p.N - 1);
+                    prefetch_l2(zrow + pc0);
+                    prefetch_l2(zrow + min(pc0 + 64, pc1));
+                    prefetch_l2(zrow + pc1);
+                }
+            }
             for (int kb = 0; kb < ge.nkb; ++kb) {
                 ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
                 if (!ok) break;

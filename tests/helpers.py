@@ -59,12 +59,14 @@ def assert_within(got, want, bound, what=""):
 def dgelu_eval_bound(z) -> np.ndarray:
     """Bound on the fp32 evaluation error of gelu'(z) in the kernel (float64
     terms): the kernel forms gelu' = s(2u) + 2 z c (1 + 3a z^2) s(2u) s(-2u) with a
-    handful of fp32 operations and one expf (documented 2 ulp); 2^-20 (8 fp32
-    ulps) of the sum of the two terms' magnitudes bounds it."""
+    handful of fp32 operations, the fast exponential intrinsic (documented error
+    2 + 1.173|x| ulp, <= 96 ulp for the clamped |x| <= 80) and the approximate
+    divide (2 ulp); 2^-16 (256 fp32 ulps) of the sum of the two terms'
+    magnitudes bounds it."""
     z = np.asarray(z, dtype=np.float64)
     c = np.sqrt(2.0 / np.pi)
     x = np.clip(2.0 * c * (z + 0.044715 * z ** 3), -80.0, 80.0)
     sp = 1.0 / (1.0 + np.exp(-x))
     sm = 1.0 - sp
     t2 = np.abs(2.0 * z * c * (1.0 + 3 * 0.044715 * z * z) * sp * sm)
-    return 2.0 ** -20 * (sp + t2) + 1e-30
+    return 2.0 ** -16 * (sp + t2) + 1e-30

@@ -48,7 +48,8 @@ def test_fprop_vs_oracle(fp8, M, N, K, epi):
     Zo, Yo = oracle.fprop_epilogue(acc, workloads.bits(bias) if epi else None, gelu_on=(epi == 2))
     y = bf16_to_f64(Y)
     gain = MAX_DGELU if epi == 2 else 1.0
-    bound = gain * FULL_C * S + bf16_ulp(np.maximum(np.abs(y), np.abs(Yo))) + 1e-6 * np.abs(Zo)
+    # last term: fp32 evaluation of gelu with the fast exponential (<= 96 ulp, 6e-6 relative)
+    bound = gain * FULL_C * S + bf16_ulp(np.maximum(np.abs(y), np.abs(Yo))) + 1e-5 * np.abs(Zo)
     assert_within(y, Yo, bound, "Y")
     if epi == 2:
         z = bf16_to_f64(Z)
