@@ -24,8 +24,10 @@
 //               warp w reads TMEM lanes 32*(w%4)..+31 (its rows) in the
 //               16x256b fragment shape, so a thread holds four rows x two
 //               columns of every 8-column chunk.  Per K block it loads its raw
-//               fp32 partial sums with two pairs of 16-lane loads, hands the
-//               buffer back to the MMA warp after the second pair and adds
+//               fp32 partial sums with four pairs of 16-lane loads (32
+//               columns each: larger loads cost the register allocator extra
+//               moves), hands the buffer back to the MMA warp after the last
+//               pair and adds
 //               sA*sB*P into a 128-element fp32 register accumulator
 //               ("promotion") with packed fp32x2 multiplies and fmas.  One
 //               8-byte column-scale load serves eight elements: the scale
@@ -61,7 +63,7 @@ constexpr int kRegsEpi = 232;
 static_assert(128 * kRegsCtrl + 128 * kEpiGroups * kRegsEpi <= kThreads * kLaunchRegs,
               "register split exceeds the pool");
 constexpr int kHalfN = kBN / kEpiGroups;  // columns per epilogue thread (128)
-static_assert(kHalfN == 128, "two 16x256b.x8 TMEM load pairs per thread and K block");
+static_assert(kHalfN == 128, "four 16x256b.x4 TMEM load pairs per thread and K block");
 constexpr int kNumAcc = 2;               // TMEM accumulator buffers
 constexpr uint32_t kTmemCols = 512;      // kNumAcc * kBN, a power of two
 static_assert(kNumAcc * kBN <= 512, "TMEM capacity");
@@ -472,18 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float* sbp = &sm.sb[ss][half * kHalfN + 2 * cq];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint64_t plo[16], phi[16];
-                    tmem_ld_16x256b_x8_pairs2(tbuf + 64u * h, tbuf + (16u << 16) + 64u * h, plo, phi);
-                    if (h == 1) {
+                for (int h = 0; h < 4; ++h) {
+                    uint64_t plo[8], phi[8];
+                    tmem_ld_16x256b_x4_pairs2(tbuf + 32u * h, tbuf + (16u << 16) + 32u * h, plo, phi);
+                    if (h == 3) {
                         // the block's partial sums are all in registers: hand the buffer back
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
                     }
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int c = 8 * h + i;
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = 4 * h + i;
                         const uint64_t sb = *reinterpret_cast<const uint64_t*>(sbp + 8 * c);
                         acc[4 * c + 0] = fma_f32x2(plo[2 * i], mul_f32x2(sa2[0], sb), acc[4 * c + 0]);
                         acc[4 * c + 1] = fma_f32x2(plo[2 * i + 1], mul_f32x2(sa2[1], sb), acc[4 * c + 1]);

@@ -200,26 +200,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32_pairs(uint32_t taddr, uint64_
         : "memory");
 }
 
-// Two 16-lane TMEM loads of 64 columns each (shape 16x256b, 8 repetitions),
+// Two 16-lane TMEM loads of 32 columns each (shape 16x256b, 4 repetitions),
 // one at lane offset +0 and one at +16 of the warp's quadrant, completed by one
 // wait inside the same statement.  Fragment of thread t for repetition i
-// (columns 8i..8i+7 from taddr): lo[2i] = row t/4, columns 8i + 2(t%4) + {0,1};
-// lo[2i+1] = row t/4 + 8, same columns; hi[] the same for rows +16.  Each
-// 64-bit value packs the even column in its low half.
-__device__ __forceinline__ void tmem_ld_16x256b_x8_pairs2(uint32_t taddr_lo, uint32_t taddr_hi, uint64_t (&lo)[16],
-                                                          uint64_t (&hi)[16]) {
+// (columns 8i..8i+7 from the address): lo[2i] = row t/4, columns
+// 8i + 2(t%4) + {0,1}; lo[2i+1] = row t/4 + 8, same columns; hi[] the same for
+// rows +16.  Each 64-bit value packs the even column in its low half.
+__device__ __forceinline__ void tmem_ld_16x256b_x4_pairs2(uint32_t a, uint32_t b, uint64_t (&lo)[8], uint64_t (&hi)[8]) {
     asm volatile(
-        "{\n\t.reg .b32 t<64>;\n\t"
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%32];\n\t"
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%33];\n\t"
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%17];\n\t"
         "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\tmov.b64 %16, {t32, t33};\n\tmov.b64 %17, {t34, t35};\n\tmov.b64 %18, {t36, t37};\n\tmov.b64 %19, {t38, t39};\n\tmov.b64 %20, {t40, t41};\n\tmov.b64 %21, {t42, t43};\n\tmov.b64 %22, {t44, t45};\n\tmov.b64 %23, {t46, t47};\n\tmov.b64 %24, {t48, t49};\n\tmov.b64 %25, {t50, t51};\n\tmov.b64 %26, {t52, t53};\n\tmov.b64 %27, {t54, t55};\n\tmov.b64 %28, {t56, t57};\n\tmov.b64 %29, {t58, t59};\n\tmov.b64 %30, {t60, t61};\n\tmov.b64 %31, {t62, t63};\n\t}"
-        : "=l"(lo[0]), "=l"(lo[1]), "=l"(lo[2]), "=l"(lo[3]), "=l"(lo[4]), "=l"(lo[5]), "=l"(lo[6]), "=l"(lo[7]), "=l"(lo[8]), "=l"(lo[9]), "=l"(lo[10]), "=l"(lo[11]), "=l"(lo[12]), "=l"(lo[13]), "=l"(lo[14]), "=l"(lo[15]),
-          "=l"(hi[0]), "=l"(hi[1]), "=l"(hi[2]), "=l"(hi[3]), "=l"(hi[4]), "=l"(hi[5]), "=l"(hi[6]), "=l"(hi[7]), "=l"(hi[8]), "=l"(hi[9]), "=l"(hi[10]), "=l"(hi[11]), "=l"(hi[12]), "=l"(hi[13]), "=l"(hi[14]), "=l"(hi[15])
-        : "r"(taddr_lo), "r"(taddr_hi)
+        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\t}"
+        : "=l"(lo[0]), "=l"(lo[1]), "=l"(lo[2]), "=l"(lo[3]), "=l"(lo[4]), "=l"(lo[5]), "=l"(lo[6]), "=l"(lo[7]), "=l"(hi[0]), "=l"(hi[1]), "=l"(hi[2]), "=l"(hi[3]), "=l"(hi[4]), "=l"(hi[5]), "=l"(hi[6]), "=l"(hi[7])
+        : "r"(a), "r"(b)
         : "memory");
 }
-
 // packed fp32x2 arithmetic on 64-bit register pairs (low half = first element);
 // each lane rounds to nearest exactly as the scalar mul / fma would
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
