@@ -212,65 +212,82 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int c
 // thread's four rows first, then across the eight lanes that hold the same
 // columns (lane xor 4, 8, 16), a fixed order, so results are deterministic --
 // and lanes 0..3 write the chunk's eight sums to the workspace band of this warp.
+// The stored pre-activations are read one chunk (4 bf16 pairs) at a time,
+// the next chunk's loads in flight while the current one is computed.
+constexpr int kZGroup = 1;
+
+__device__ __forceinline__ void load_z_group(const GemmParams& p, const uint16_t* zp, bool pairs, int row0, int col0,
+                                             int c0, uint32_t (&zw)[4 * kZGroup]) {
+#pragma unroll
+    for (int i = 0; i < kZGroup; ++i) {
+        const int col = col0 + 8 * (c0 + i);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + 8 * r;
+            uint32_t w = 0u;
+            if (row < p.M && col < p.N) {
+                const int64_t off = static_cast<int64_t>(row) * p.N + col;
+                if (pairs)
+                    w = *reinterpret_cast<const uint32_t*>(zp + off);
+                else
+                    w = static_cast<uint32_t>(zp[off]) |
+                        (col + 1 < p.N ? static_cast<uint32_t>(zp[off + 1]) << 16 : 0u);
+            }
+            zw[4 * i + r] = w;
+        }
+    }
+}
+
 template <bool BGRAD>
 __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int col0,
                                             const uint64_t (&acc)[4 * kChunks], float* band, int lane) {
     const bool pairs = (p.N & 1) == 0;
     uint16_t* out = static_cast<uint16_t*>(p.out);
     const uint16_t* zp = static_cast<const uint16_t*>(p.aux);
-    // all of the thread's stored pre-activations first (bf16 pairs), so that
-    // the loads are in flight together
-    uint32_t zw[4 * kChunks];
+    uint32_t zcur[4 * kZGroup], znext[4 * kZGroup];
+    load_z_group(p, zp, pairs, row0, col0, 0, zcur);
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        const int col = col0 + 8 * c;
+    for (int c0 = 0; c0 < kChunks; c0 += kZGroup) {
+        if (c0 + kZGroup < kChunks) load_z_group(p, zp, pairs, row0, col0, c0 + kZGroup, znext);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int row = row0 + 8 * r;
-            zw[4 * c + r] = 0u;
-            if (row < p.M && col < p.N) {
+        for (int i = 0; i < kZGroup; ++i) {
+            const int c = c0 + i;
+            const int col = col0 + 8 * c;
+            const bool one = col < p.N, two = col + 1 < p.N;
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = row0 + 8 * r;
+                if (row >= p.M || !one) continue;
+                const float2 a = unpack_f32x2(acc[4 * c + r]);
                 const int64_t off = static_cast<int64_t>(row) * p.N + col;
-                if (pairs)
-                    zw[4 * c + r] = *reinterpret_cast<const uint32_t*>(zp + off);
-                else
-                    zw[4 * c + r] = static_cast<uint32_t>(zp[off]) |
-                                    (col + 1 < p.N ? static_cast<uint32_t>(zp[off + 1]) << 16 : 0u);
+                const float z0 = bf16_lo(zcur[4 * i + r]), z1 = bf16_hi(zcur[4 * i + r]);
+                const float d0 = a.x * dgelu_tanh(z0);
+                const float d1 = two ? a.y * dgelu_tanh(z1) : 0.0f;
+                if (pairs) {
+                    *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(d0, d1);
+                } else {
+                    out[off] = static_cast<uint16_t>(pack_bf16x2(d0, 0.0f) & 0xFFFFu);
+                    if (two) out[off + 1] = static_cast<uint16_t>(pack_bf16x2(d1, 0.0f) & 0xFFFFu);
+                }
+                s0 += d0;
+                s1 += d1;
+            }
+            if (BGRAD) {
+#pragma unroll
+                for (int m = 4; m <= 16; m <<= 1) {
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, m);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, m);
+                }
+                if (lane < 4) {
+                    if (one) band[col] = s0;
+                    if (two) band[col + 1] = s1;
+                }
             }
         }
-    }
+        if (c0 + kZGroup < kChunks) {
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        const int col = col0 + 8 * c;
-        const bool one = col < p.N, two = col + 1 < p.N;
-        float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int row = row0 + 8 * r;
-            if (row >= p.M || !one) continue;
-            const float2 a = unpack_f32x2(acc[4 * c + r]);
-            const int64_t off = static_cast<int64_t>(row) * p.N + col;
-            const float z0 = bf16_lo(zw[4 * c + r]), z1 = bf16_hi(zw[4 * c + r]);
-            const float d0 = a.x * dgelu_tanh(z0);
-            const float d1 = two ? a.y * dgelu_tanh(z1) : 0.0f;
-            if (pairs) {
-                *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(d0, d1);
-            } else {
-                out[off] = static_cast<uint16_t>(pack_bf16x2(d0, 0.0f) & 0xFFFFu);
-                if (two) out[off + 1] = static_cast<uint16_t>(pack_bf16x2(d1, 0.0f) & 0xFFFFu);
-            }
-            s0 += d0;
-            s1 += d1;
-        }
-        if (BGRAD) {
-#pragma unroll
-            for (int m = 4; m <= 16; m <<= 1) {
-                s0 += __shfl_xor_sync(0xffffffffu, s0, m);
-                s1 += __shfl_xor_sync(0xffffffffu, s1, m);
-            }
-            if (lane < 4) {
-                if (one) band[col] = s0;
-                if (two) band[col + 1] = s1;
-            }
+            for (int j = 0; j < 4 * kZGroup; ++j) zcur[j] = znext[j];
         }
     }
 }
