@@ -35,6 +35,36 @@ SEED = 1002  # base seed of the training-step workload
 WORKLOAD = "linear_train_step_m8192_k4096_n14336_bias_gelu"
 METRIC = "FP8 GEMM TFLOPS (fprop/dgrad/wgrad) and % of GB300 dense-FP8 peak, 1 GPU"
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor-core ratio on this part
+KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "common.cuh", "internal.h", "gemm_fprop.cu", "gemm_dgrad.cu",
+                  "gemm_wgrad.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fp8_kernel_m8192_k4096_n14336_traffic.md")
+
+
+def kernel_source_digest():
+    """sha256 over the GEMM kernel's source files (the DRAM-traffic summary
+    applies only to the build it was measured on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "fp8_linear_layer_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum,
+    averaged over the step's three launches) from the committed ncu summary,
+    or None when the kernel sources changed since it was taken."""
+    import re
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    sha = re.search(r"sources_sha256:\s*([0-9a-f]{64})", text)
+    val = re.search(r"bytes_per_launch:\s*([0-9]+)", text)
+    if not sha or not val or sha.group(1) != kernel_source_digest():
+        return None
+    return int(val.group(1))
 
 
 def parse_args():
@@ -49,7 +79,7 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k"], default=None,
+    ap.add_argument("--study", choices=["long_k", "kernels"], default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
     ap.add_argument("--study-k", type=int, default=16384)
@@ -359,7 +389,8 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "kernel": "gemm_fp8_kernel (fprop, dgrad, wgrad launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),
-                         "traffic": None, "avg_gemm_ms": avg_gemm_ms},
+                         "traffic": measured_traffic() if default_size else None, "traffic_unit": "bytes",
+                         "avg_gemm_ms": avg_gemm_ms},
             "e2e": e2e,
             "gpu_launches": step.KERNELS_PER_STEP * args.steps,
             "clocks": clk,
@@ -439,10 +470,69 @@ def run_long_k_study(args):
     return 0
 
 
+def run_kernel_study(args):
+    """Per-launch speed of every kernel of the training step (m, k, n from the
+    command line) plus the dense weight-gradient table's largest shape and a
+    long-K weight gradient: CUDA events around `reps` launches after 3 warm-ups;
+    GEMMs in TFLOP/s (2 M N K per launch), casts in GB/s of algorithmic bytes
+    (2 read + 1 written + 4/128 of scale per element)."""
+    import torch
+    import workloads
+    import fp8_linear_layer_gb300 as fp8
+    reps = 10
+    m, k, n = args.m, args.k, args.n
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps
+
+    out = {"study": "kernels", "reps": reps, "gemm_tflops": {}, "cast_gbs": {}}
+    x = workloads.normal_bf16((m, k), SEED, "X").cuda()
+    w = workloads.normal_bf16((n, k), SEED, "W", std=0.02).cuda()
+    bias = workloads.normal_bf16((n,), SEED, "b", std=0.02).cuda()
+    dy = workloads.normal_bf16((m, k), SEED, "dY", std=1e-2).cuda()
+    X, W, DY = fp8.quantize(x, fp8.E4M3), fp8.quantize(w, fp8.E4M3), fp8.quantize(dy, fp8.E5M2)
+    Y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    Z, dZ = torch.empty_like(Y), torch.empty_like(Y)
+    f = 2.0 * m * n * k / 1e9
+    out["gemm_tflops"]["fprop_bias_gelu_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.gemm_fprop(X, W, bias, fp8.EPI_BIAS_GELU, out=Y, aux=Z))
+    out["gemm_tflops"]["dgrad_dgelu_bgrad_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.gemm_dgrad(DY, W, Z, fp8.EPI_DGELU_BGRAD, out=dZ))
+    DZT, XT = fp8.quantize(dZ, fp8.E5M2, transpose=True), fp8.quantize(x, fp8.E4M3, transpose=True)
+    dW = torch.zeros((n, k), device="cuda")
+    out["gemm_tflops"]["wgrad_accumulate_m%d_n%d_k%d" % (n, k, m)] = f / timed(lambda: fp8.gemm_wgrad(DZT, XT, dW))
+    for (M, N, K) in ((16384, 7168, 8192), (8192, 8192, 16384)):
+        a = fp8.quantize(workloads.normal_bf16((M, K), SEED + 1, "A", std=0.02).cuda(), fp8.E4M3)
+        bq = fp8.quantize(workloads.normal_bf16((N, K), SEED + 1, "B", std=0.02).cuda(), fp8.E4M3)
+        o = torch.zeros((M, N), device="cuda")
+        out["gemm_tflops"]["wgrad_accumulate_m%d_n%d_k%d" % (M, N, K)] = 2.0 * M * N * K / 1e9 / timed(
+            lambda: fp8.gemm_wgrad(a, bq, o))
+        del a, bq, o
+    xb = workloads.normal_bf16((32768, 8192), SEED + 2, "C").cuda()
+    gb = xb.numel() * (3.0 + 4.0 / 128) / 1e6
+    for fmt, nm in ((fp8.E4M3, "e4m3"), (fp8.E5M2, "e5m2")):
+        out["cast_gbs"]["rows_%s_32768x8192" % nm] = gb / timed(lambda: fp8.quantize(xb, fmt))
+        out["cast_gbs"]["transposed_%s_32768x8192" % nm] = gb / timed(lambda: fp8.quantize(xb, fmt, transpose=True))
+    out["hbm_peak_gbs"] = peaks()[1]
+    out["status"] = fp8.device_status()
+    print(json.dumps(out))
+
+
 def main():
     args = parse_args()
     if args.study == "long_k":
         return run_long_k_study(args)
+    if args.study == "kernels":
+        return run_kernel_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

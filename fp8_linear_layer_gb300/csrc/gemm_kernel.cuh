@@ -155,7 +155,10 @@ __device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, 
     }
 }
 
-// fprop: Z = acc + bias[j]; Y = gelu(Z) or Z; bf16 out (+ bf16 aux Z)
+// fprop: Z = acc + bias[j]; Y = gelu(Z) or Z; bf16 out (+ bf16 aux Z).
+// Each chunk's eight values are computed without branches (rows or columns
+// outside the matrix compute on zeros) so that their independent GELU
+// evaluations overlap; only the memory accesses are guarded.
 template <int EPI>
 __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int col0,
                                             const uint64_t (&acc)[4 * kChunks]) {
@@ -180,27 +183,32 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int c
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         const int col = col0 + 8 * c;
-        if (col >= p.N) continue;
-        const bool two = col + 1 < p.N;
+        const bool one = col < p.N, two = col + 1 < p.N;
         const float b0 = bf16_lo(bw[c]), b1 = bf16_hi(bw[c]);
+        uint32_t yw[4], zw[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int row = row0 + 8 * r;
-            if (row >= p.M) continue;
             const float2 a = unpack_f32x2(acc[4 * c + r]);
             const float z0 = a.x + b0, z1 = a.y + b1;
             const float y0 = (EPI == kEpiBiasGelu) ? gelu_tanh(z0) : z0;
             const float y1 = (EPI == kEpiBiasGelu) ? gelu_tanh(z1) : z1;
+            yw[r] = pack_bf16x2(y0, y1);
+            zw[r] = pack_bf16x2(z0, z1);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + 8 * r;
+            if (row >= p.M || !one) continue;
             const int64_t off = static_cast<int64_t>(row) * p.N + col;
             if (pairs) {
-                *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(y0, y1);
-                if (aux) *reinterpret_cast<uint32_t*>(aux + off) = pack_bf16x2(z0, z1);
+                *reinterpret_cast<uint32_t*>(out + off) = yw[r];
+                if (aux) *reinterpret_cast<uint32_t*>(aux + off) = zw[r];
             } else {
-                out[off] = static_cast<uint16_t>(pack_bf16x2(y0, 0.0f) & 0xFFFFu);
-                if (aux) aux[off] = static_cast<uint16_t>(pack_bf16x2(z0, 0.0f) & 0xFFFFu);
+                out[off] = static_cast<uint16_t>(yw[r] & 0xFFFFu);
+                if (aux) aux[off] = static_cast<uint16_t>(zw[r] & 0xFFFFu);
                 if (two) {
-                    out[off + 1] = static_cast<uint16_t>(pack_bf16x2(y1, 0.0f) & 0xFFFFu);
-                    if (aux) aux[off + 1] = static_cast<uint16_t>(pack_bf16x2(z1, 0.0f) & 0xFFFFu);
+                    out[off + 1] = static_cast<uint16_t>(yw[r] >> 16);
+                    if (aux) aux[off + 1] = static_cast<uint16_t>(zw[r] >> 16);
                 }
             }
         }
@@ -254,24 +262,30 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
             const int c = c0 + i;
             const int col = col0 + 8 * c;
             const bool one = col < p.N, two = col + 1 < p.N;
+            // all eight values first, without branches (outside the matrix the
+            // stored pre-activation reads as zero and the value is masked below)
+            float d[4][2];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float2 a = unpack_f32x2(acc[4 * c + r]);
+                d[r][0] = a.x * dgelu_tanh(bf16_lo(zcur[4 * i + r]));
+                d[r][1] = a.y * dgelu_tanh(bf16_hi(zcur[4 * i + r]));
+            }
             float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int row = row0 + 8 * r;
-                if (row >= p.M || !one) continue;
-                const float2 a = unpack_f32x2(acc[4 * c + r]);
+                const bool ok = row < p.M && one;
+                s0 += ok ? d[r][0] : 0.0f;
+                s1 += (ok && two) ? d[r][1] : 0.0f;
+                if (!ok) continue;
                 const int64_t off = static_cast<int64_t>(row) * p.N + col;
-                const float z0 = bf16_lo(zcur[4 * i + r]), z1 = bf16_hi(zcur[4 * i + r]);
-                const float d0 = a.x * dgelu_tanh(z0);
-                const float d1 = two ? a.y * dgelu_tanh(z1) : 0.0f;
                 if (pairs) {
-                    *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(d0, d1);
+                    *reinterpret_cast<uint32_t*>(out + off) = pack_bf16x2(d[r][0], d[r][1]);
                 } else {
-                    out[off] = static_cast<uint16_t>(pack_bf16x2(d0, 0.0f) & 0xFFFFu);
-                    if (two) out[off + 1] = static_cast<uint16_t>(pack_bf16x2(d1, 0.0f) & 0xFFFFu);
+                    out[off] = static_cast<uint16_t>(pack_bf16x2(d[r][0], 0.0f) & 0xFFFFu);
+                    if (two) out[off + 1] = static_cast<uint16_t>(pack_bf16x2(d[r][1], 0.0f) & 0xFFFFu);
                 }
-                s0 += d0;
-                s1 += d1;
             }
             if (BGRAD) {
 #pragma unroll
