@@ -64,13 +64,17 @@ __device__ __forceinline__ uint2 encode8(const float (&f)[8], float inv) {
 // ------------------------------------------------------------------ row-wise
 // A half-warp owns one (row, 128-block) task: 16 lanes x 16 bytes of bf16.
 // Consecutive tasks are consecutive blocks of a row, so a warp reads 512
-// contiguous bytes.  Each warp keeps U task pairs in flight.
-template <int FMT, int U>
+// contiguous bytes.  Each warp keeps U task pairs in flight.  When the rows
+// are packed (ldx == cols) the flat task index addresses input and output
+// directly; the (row, block) split -- a division -- is needed only for the
+// scale, by one lane per task, in 32-bit arithmetic when the task count fits.
+template <int FMT, int U, bool PACKED>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
                                                             float* __restrict__ scale, int64_t sld) {
     const int64_t nb = cols / 128;
     const int64_t total = rows * nb;
+    const bool small = total <= 0xFFFFFFFFll;
     const int lane = threadIdx.x & 31;
     const int hl = lane & 15;
     const int hw = lane >> 4;
@@ -79,19 +83,24 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 
     for (int64_t base = warp * 2 * U; base < total; base += nwarps * 2 * U) {
         uint4 v[U];
-        int64_t task[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            task[u] = base + 2 * u + hw;
+            const int64_t task = base + 2 * u + hw;
             v[u] = make_uint4(0, 0, 0, 0);
-            if (task[u] < total) {
-                const int64_t r = task[u] / nb;
-                const int64_t b = task[u] - r * nb;
-                v[u] = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + b * 128 + hl * 8));
+            if (task < total) {
+                const uint16_t* src;
+                if (PACKED) {
+                    src = x + task * 128 + hl * 8;
+                } else {
+                    const int64_t r = task / nb;
+                    src = x + r * ldx + (task - r * nb) * 128 + hl * 8;
+                }
+                v[u] = __ldcs(reinterpret_cast<const uint4*>(src));
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int64_t task = base + 2 * u + hw;
             float f[8];
             f[0] = bf16_lo(v[u].x); f[1] = bf16_hi(v[u].x);
             f[2] = bf16_lo(v[u].y); f[3] = bf16_hi(v[u].y);
@@ -105,11 +114,22 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
             float inv, s;
             block_scale<FMT>(amax, inv, s);
             const uint2 codes = encode8<FMT>(f, inv);
-            if (task[u] < total) {
-                const int64_t r = task[u] / nb;
-                const int64_t b = task[u] - r * nb;
-                *reinterpret_cast<uint2*>(q + r * cols + b * 128 + hl * 8) = codes;
-                if (hl == 0) scale[b * sld + r] = s;
+            if (task < total) {
+                // q is always packed: row r, block b starts at (r * nb + b) * 128 = task * 128
+                *reinterpret_cast<uint2*>(q + task * 128 + hl * 8) = codes;
+                if (hl == 0) {
+                    int64_t r, b;
+                    if (small) {
+                        const uint32_t t32 = static_cast<uint32_t>(task), nb32 = static_cast<uint32_t>(nb);
+                        const uint32_t r32 = t32 / nb32;
+                        r = r32;
+                        b = t32 - r32 * nb32;
+                    } else {
+                        r = task / nb;
+                        b = task - r * nb;
+                    }
+                    scale[b * sld + r] = s;
+                }
             }
         }
     }
@@ -122,7 +142,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // each 32-row band rotated by 8 words so that the column-wise reads of the
 // four 32-row parts hit 32 distinct banks.
 template <int FMT>
-__global__ void __launch_bounds__(256) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
                                                             float* __restrict__ scale, int64_t sld) {
     __shared__ __align__(16) uint32_t tile[128][64];
@@ -145,15 +165,15 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const uint16_t* __re
     const int cp = threadIdx.x >> 2;  // column pair 0..63
     const int p = threadIdx.x & 3;    // 32-row part
     const int64_t c = c0 + 2 * cp;
-    float lo[32], hi[32];
+    // two passes over the staged tile (amax, then encode) instead of holding
+    // 64 values in registers: the lower register count keeps more tiles, and
+    // so more loads, in flight per SM
     float amax_lo = 0.0f, amax_hi = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
-        lo[i] = bf16_lo(w);
-        hi[i] = bf16_hi(w);
-        amax_lo = fmaxf(amax_lo, fabsf(lo[i]));
-        amax_hi = fmaxf(amax_hi, fabsf(hi[i]));
+        amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
+        amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
     }
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
@@ -167,12 +187,16 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const uint16_t* __re
         uint32_t wl[8], wh[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t a = Fp8Fmt<FMT>::cvt2(__fmul_rn(lo[4 * i], inv_lo), __fmul_rn(lo[4 * i + 1], inv_lo));
-            const uint32_t b = Fp8Fmt<FMT>::cvt2(__fmul_rn(lo[4 * i + 2], inv_lo), __fmul_rn(lo[4 * i + 3], inv_lo));
-            wl[i] = a | (b << 16);
-            const uint32_t d = Fp8Fmt<FMT>::cvt2(__fmul_rn(hi[4 * i], inv_hi), __fmul_rn(hi[4 * i + 1], inv_hi));
-            const uint32_t e = Fp8Fmt<FMT>::cvt2(__fmul_rn(hi[4 * i + 2], inv_hi), __fmul_rn(hi[4 * i + 3], inv_hi));
-            wh[i] = d | (e << 16);
+            uint32_t lo16[2], hi16[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t w0 = tile[32 * p + 4 * i + 2 * k][(cp + 8 * p) & 63];
+                const uint32_t w1 = tile[32 * p + 4 * i + 2 * k + 1][(cp + 8 * p) & 63];
+                lo16[k] = Fp8Fmt<FMT>::cvt2(__fmul_rn(bf16_lo(w0), inv_lo), __fmul_rn(bf16_lo(w1), inv_lo));
+                hi16[k] = Fp8Fmt<FMT>::cvt2(__fmul_rn(bf16_hi(w0), inv_hi), __fmul_rn(bf16_hi(w1), inv_hi));
+            }
+            wl[i] = lo16[0] | (lo16[1] << 16);
+            wh[i] = hi16[0] | (hi16[1] << 16);
         }
         uint4* dl = reinterpret_cast<uint4*>(q + c * rows + r0 + 32 * p);
         uint4* dh = reinterpret_cast<uint4*>(q + (c + 1) * rows + r0 + 32 * p);
@@ -216,12 +240,19 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
         const int64_t cap = static_cast<int64_t>(num_sms) * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        if (fmt == 0)
-            quantize_rows_kernel<0, U><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(xb, rows, cols, ldx, q,
-                                                                                           scale, sld);
-        else
-            quantize_rows_kernel<1, U><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(xb, rows, cols, ldx, q,
-                                                                                           scale, sld);
+        const unsigned g = static_cast<unsigned>(blocks);
+        const bool packed = ldx == cols;
+        if (fmt == 0) {
+            if (packed)
+                quantize_rows_kernel<0, U, true><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+            else
+                quantize_rows_kernel<0, U, false><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+        } else {
+            if (packed)
+                quantize_rows_kernel<1, U, true><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+            else
+                quantize_rows_kernel<1, U, false><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+        }
     } else {
         dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
         if (fmt == 0)
