@@ -79,7 +79,7 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k", "kernels"], default=None,
+    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak"], default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
     ap.add_argument("--study-k", type=int, default=16384)
@@ -527,12 +527,63 @@ def run_kernel_study(args):
     print(json.dumps(out))
 
 
+def run_fp8_peak_probe(args):
+    """Dense fp8 tensor-core throughput of the vendor library on this GPU, for
+    context beside the roofline denominator (which stays the measured bf16
+    burst x the nominal ratio): torch._scaled_mm, e4m3 x e4m3 -> bf16 with
+    per-tensor scales, 8192^3, best of 10 (burst) and back to back for ~4 s
+    (sustained).  A probe outside the measured path: none of this library's
+    kernels run here."""
+    import torch
+    n = 8192
+    g = torch.Generator(device="cuda").manual_seed(SEED)
+    a = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn).t()  # column-major operand
+    one = torch.ones((), device="cuda")
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        mm()
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    flops = 2.0 * n ** 3
+    clocks = ClockSampler(0)
+    clocks.start()
+    reps, t0 = 0, time.time()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    while time.time() - t0 < 4.0:
+        for _ in range(20):
+            mm()
+        reps += 20
+        torch.cuda.synchronize()
+    e.record()
+    e.synchronize()
+    clk = clocks.stop()
+    out = {"study": "fp8_peak", "op": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3",
+           "burst_tflops": flops / best / 1e9, "sustained_tflops": flops * reps / s.elapsed_time(e) / 1e9,
+           "sustained_seconds": round(time.time() - t0, 2), "clocks": clk,
+           "bf16_measured_x2": peaks()[0]}
+    print(json.dumps(out))
+
+
 def main():
     args = parse_args()
     if args.study == "long_k":
         return run_long_k_study(args)
     if args.study == "kernels":
         return run_kernel_study(args)
+    if args.study == "fp8_peak":
+        return run_fp8_peak_probe(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

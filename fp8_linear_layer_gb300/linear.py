@@ -15,6 +15,9 @@ should use fast accumulation") and the accumulating fp32 weight gradient of
     dgrad:  dZ = (dYq Wq^T) * gelu'(Z),  db = sum_tokens dZ      (bf16 dZ, fp32 db)
     dZ^T --quantize down columns, e5m2-->  (n x m)     X^T --columns, e4m3--> (k x m)
     wgrad:  dW (n x k, fp32) += dZ^T X    (contraction over the m tokens)
+    input gradient (optional, ``input_grad``):
+            dZ --rows, e5m2--> dZq (m x n)    W --down columns, e4m3--> W^T (k x n)
+            dX = dZq (W^T)^T = dZ W        (bf16, m x k, contraction over the n features)
 
 All buffers are allocated once (torch) so a step launches 9 kernels and
 allocates nothing; ``step`` can be captured in a CUDA graph.
@@ -61,6 +64,22 @@ class LinearTrainStep:
         B.quantize(X, B.E4M3, transpose=True, out=self.XTq)
         B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)
         return self.dW, self.db
+
+    def input_grad(self, W):
+        """dX = dZ W (m x k, bf16), the gradient passed on to the layer's input:
+        the backward GEMM of "How can we use te.Linear with weight parallel?"
+        that contracts over the output features.  Both operands are cast with
+        their 128-blocks along n (dZ by rows, W down its columns), so the GEMM is
+        the plain NT form without an epilogue.  Needs ``backward`` first."""
+        if not hasattr(self, "dX"):
+            dev = self.dZ.device
+            self.dZq = B.empty_fp8(self.m, self.n, B.E5M2, dev)
+            self.WTq = B.empty_fp8(self.k, self.n, B.E4M3, dev)
+            self.dX = torch.empty((self.m, self.k), dtype=torch.bfloat16, device=dev)
+        B.quantize(self.dZ, B.E5M2, out=self.dZq)
+        B.quantize(W, B.E4M3, transpose=True, out=self.WTq)
+        B.gemm_fprop(self.dZq, self.WTq, None, B.EPI_NONE, self.acc_mode, out=self.dX)
+        return self.dX
 
     def step(self, X, W, b, dY):
         self.forward(X, W, b)

@@ -1,0 +1,54 @@
+"""The layer's input gradient dX = dZ W (bf16, m x k) through the C ABI vs the
+oracle: dZ cast by rows (e5m2, blocks along the n output features), W cast
+down its columns (e4m3, blocks along n) to the k x n operand, then the plain
+NT GEMM without an epilogue -- the backward GEMM that contracts over the
+output features ("How can we use te.Linear with weight parallel?").
+
+Bound: |gpu - oracle| <= 2e-3 * S (S = sum_n |dz_in w_nk| of the dequantized
+operands) + one bf16 ulp.  Shapes with ragged m and k.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import FULL_C, assert_within, bf16_to_f64, bf16_ulp
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = 0, 1
+
+
+@pytest.mark.parametrize("m,k,n", [(300, 264, 384), (129, 1000, 256), (1024, 520, 640)])
+def test_input_grad_vs_oracle(fp8, m, k, n):
+    dz = workloads.normal_bf16((m, n), 71, "dz", std=1e-2)
+    w = workloads.normal_bf16((n, k), 71, "w", std=0.02)
+    A = fp8.quantize(dz.cuda(), E5M2)
+    Bt = fp8.quantize(w.cuda(), E4M3, transpose=True)
+    assert Bt.q.shape == (k, n)
+    dX, _ = fp8.gemm_fprop(A, Bt, None, fp8.EPI_NONE)
+    torch.cuda.synchronize()
+    assert dX.shape == (m, k)
+    qa, sa = oracle.quantize(workloads.bits(dz), E5M2)
+    qb, sb = oracle.quantize(workloads.bits(w), E4M3, transpose=True)
+    acc, S = oracle.gemm(qa, sa, E5M2, qb, sb, E4M3)
+    got = bf16_to_f64(dX)
+    assert_within(got, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(got), np.abs(acc))), "dX")
+
+
+def test_train_step_input_grad_matches_direct_call(fp8):
+    # the driver's dX is the same GEMM on the same casts: bit-identical
+    from fp8_linear_layer_gb300.linear import LinearTrainStep
+    m, k, n = 256, 384, 512
+    X = workloads.normal_bf16((m, k), 72, "x").cuda()
+    W = workloads.normal_bf16((n, k), 72, "w", std=0.02).cuda()
+    b = workloads.normal_bf16((n,), 72, "b", std=0.02).cuda()
+    dY = workloads.normal_bf16((m, k), 72, "dy", std=1e-2).cuda()
+    step = LinearTrainStep(m, k, n)
+    step.step(X, W, b, dY)
+    dX = step.input_grad(W).clone()
+    A = fp8.quantize(step.dZ, E5M2)
+    Bt = fp8.quantize(W, E4M3, transpose=True)
+    ref, _ = fp8.gemm_fprop(A, Bt, None, fp8.EPI_NONE)
+    torch.cuda.synchronize()
+    assert torch.equal(dX, ref)
