@@ -79,7 +79,7 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak"], default=None,
+    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables"], default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
     ap.add_argument("--study-k", type=int, default=16384)
@@ -557,6 +557,53 @@ def run_kernel_study(args):
     print(json.dumps(out))
 
 
+def run_wgrad_tables(args):
+    """The weight-gradient tables: the dense sweep (six (M, N) shapes x K in
+    {4096, 8192}, fp32 out += A B^T) and the k-grouped MoE table (G experts,
+    per-expert token counts drawn multinomially and rounded to multiples of 128,
+    zero groups allowed), each timed with CUDA events around 10 launches after
+    3 warm-ups.  Operands are random on the device (values do not change the
+    timing); TFLOP/s = sum over groups of 2 M N K_g per launch."""
+    import torch
+    import workloads
+    import fp8_linear_layer_gb300 as fp8
+    reps = 10
+    g = torch.Generator(device="cuda").manual_seed(SEED)
+
+    def operand(rows, k):
+        return fp8.quantize((torch.randn(rows, k, device="cuda", generator=g) * 0.02).to(torch.bfloat16), fp8.E4M3)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps
+
+    dense, grouped = {}, {}
+    for K in workloads.DENSE_WGRAD_K:
+        for (M, N) in workloads.DENSE_WGRAD_MN:
+            A, Bq = operand(M, K), operand(N, K)
+            out = torch.zeros((M, N), device="cuda")
+            dense["m%d_n%d_k%d" % (M, N, K)] = 2.0 * M * N * K / 1e9 / timed(lambda: fp8.gemm_wgrad(A, Bq, out))
+            del A, Bq, out
+    for i, (G, M, N, per) in enumerate(workloads.GROUPED_WGRAD):
+        ks = workloads.moe_group_sizes(G, G * per, SEED + i)
+        tot = sum(ks)
+        A, Bq = operand(M, tot), operand(N, tot)
+        out = torch.zeros((G, M, N), device="cuda")
+        grouped["g%d_m%d_n%d_tokens%d" % (G, M, N, tot)] = {
+            "k_sizes": ks, "tflops": 2.0 * M * N * tot / 1e9 / timed(lambda: fp8.grouped_wgrad(A, Bq, ks, out))}
+        del A, Bq, out
+    print(json.dumps({"study": "wgrad_tables", "reps": reps, "dense_tflops": dense, "grouped": grouped,
+                      "status": fp8.device_status()}))
+
+
 def run_fp8_peak_probe(args):
     """Dense fp8 tensor-core throughput of the vendor library on this GPU, for
     context beside the roofline denominator (which stays the measured bf16
@@ -614,6 +661,8 @@ def main():
         return run_kernel_study(args)
     if args.study == "fp8_peak":
         return run_fp8_peak_probe(args)
+    if args.study == "wgrad_tables":
+        return run_wgrad_tables(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
