@@ -58,6 +58,8 @@ def _load():
         lib.oracle_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, vp, i64]
         lib.oracle_gemm.argtypes = [i64, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64, i32,
                                     vp, i64, vp, i64, vp, vp]
+        lib.oracle_mx_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, vp, i64]
+        lib.oracle_mx_gemm.argtypes = [i64, vp, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp, i64, vp, vp]
         lib.oracle_gelu.argtypes = [ctypes.c_double]
         lib.oracle_gelu.restype = ctypes.c_double
         lib.oracle_dgelu.argtypes = [ctypes.c_double]
@@ -175,6 +177,55 @@ def gemm(qa, sa, fmt_a, qb, sb, fmt_b, K=None, k0=0, rows=None, cols=None, want_
                         _p(qb), ldb, _p(sb), sb.shape[1], int(fmt_b),
                         None if r is None else _p(r), nr, None if c is None else _p(c), nc,
                         _p(acc), None if S is None else _p(S))
+    return acc, S
+
+
+# ----------------------------------------------------------------- MXFP8 ----
+
+def mx_quantize(x_bits, fmt: int, transpose: bool = False):
+    """MXFP8 cast of a bf16 matrix (bit patterns, [rows][cols]): one power-of-two
+    scale 2^e per 32 elements, e the smallest integer in [-127, 127] with
+    amax <= FMAX 2^e (0 for an all-zero block), codes enc(x 2^-e).
+
+    transpose=False: blocks along each row; returns q [rows][cols] (uint8) and
+      e [cols/32][rows] (int8).
+    transpose=True: blocks down each column; returns q [cols][rows] and
+      e [rows/32][cols].
+    """
+    x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
+    rows, cols = x.shape
+    if not transpose:
+        assert cols % 32 == 0
+        q = np.empty((rows, cols), dtype=np.uint8)
+        e = np.empty((cols // 32, rows), dtype=np.int8)
+        _load().oracle_mx_quantize(int(fmt), _p(x), rows, cols, cols, 0, _p(q), _p(e), rows)
+    else:
+        assert rows % 32 == 0
+        q = np.empty((cols, rows), dtype=np.uint8)
+        e = np.empty((rows // 32, cols), dtype=np.int8)
+        _load().oracle_mx_quantize(int(fmt), _p(x), rows, cols, cols, 1, _p(q), _p(e), cols)
+    return q, e
+
+
+def mx_gemm(qa, ea, fmt_a, qb, eb, fmt_b, rows=None, cols=None, want_abs=True):
+    """MXFP8 "nt" GEMM in float64: acc[i][j] = sum_k dec(qa[i,k]) 2^ea[k/32,i] *
+    dec(qb[j,k]) 2^eb[k/32,j]; returns (acc, S) with S the sum of |products|."""
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qb = np.ascontiguousarray(qb, dtype=np.uint8)
+    ea = np.ascontiguousarray(ea, dtype=np.int8)
+    eb = np.ascontiguousarray(eb, dtype=np.int8)
+    M, K = qa.shape
+    N, K2 = qb.shape
+    assert K == K2 and K % 32 == 0 and ea.shape[0] == K // 32 and eb.shape[0] == K // 32
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if c is None else c.size
+    acc = np.empty((nr, nc), dtype=np.float64)
+    S = np.empty((nr, nc), dtype=np.float64) if want_abs else None
+    _load().oracle_mx_gemm(K, _p(qa), K, _p(ea), ea.shape[1], int(fmt_a), _p(qb), K, _p(eb), eb.shape[1],
+                           int(fmt_b), None if r is None else _p(r), nr, None if c is None else _p(c), nc,
+                           _p(acc), None if S is None else _p(S))
     return acc, S
 
 

@@ -284,6 +284,95 @@ void oracle_gemm(int64_t K, int64_t k0,
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8: power-of-two scales per 32 elements (the MX block format named among */
+/* the fp8 recipes on "How can we use te.Linear with weight parallel?")       */
+/* ------------------------------------------------------------------------ */
+
+/* Smallest integer e in [-127, 127] with amax <= FMAX * 2^e (so that no element
+ * of the block saturates); 0 for an all-zero block.  Found by stepping e one
+ * power of two at a time with exact binary64 comparisons. */
+static int mx_exponent(int fmt, double amax)
+{
+    const double fmax = oracle_fp8_max(fmt);
+    if (amax == 0.0) return 0;
+    int e = 0;
+    while (e < 127 && amax > ldexp(fmax, e)) ++e;
+    while (e > -127 && amax <= ldexp(fmax, e - 1)) --e;
+    return e;
+}
+
+/* One 32-element block: exponent, then q_k = enc(x_k * 2^-e) (the scaling by a
+ * power of two is exact, so this is a single rounding of x_k * 2^-e). */
+static void mx_block(int fmt, const float* v, uint8_t* q, int64_t qstride, int8_t* e_out)
+{
+    double amax = 0.0;
+    for (int k = 0; k < 32; ++k) {
+        const double a = fabs((double)v[k]);
+        if (a > amax) amax = a;
+    }
+    const int e = mx_exponent(fmt, amax);
+    for (int k = 0; k < 32; ++k) q[k * qstride] = oracle_fp8_encode(fmt, (float)ldexp((double)v[k], -e));
+    *e_out = (int8_t)e;
+}
+
+void oracle_mx_quantize(int fmt, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                        int transpose, uint8_t* q, int8_t* e, int64_t eld)
+{
+    build_tables();
+    if (!transpose) {
+        const int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            float v[32];
+            for (int64_t b = 0; b < nb; ++b) {
+                for (int k = 0; k < 32; ++k) v[k] = oracle_bf16_to_f32(x[r * ldx + b * 32 + k]);
+                mx_block(fmt, v, q + r * cols + b * 32, 1, &e[b * eld + r]);
+            }
+        }
+    } else {
+        const int64_t nb = rows / 32;
+#pragma omp parallel for schedule(static)
+        for (int64_t c = 0; c < cols; ++c) {
+            float v[32];
+            for (int64_t b = 0; b < nb; ++b) {
+                for (int k = 0; k < 32; ++k) v[k] = oracle_bf16_to_f32(x[(b * 32 + k) * ldx + c]);
+                mx_block(fmt, v, q + c * rows + b * 32, 1, &e[b * eld + c]);
+            }
+        }
+    }
+}
+
+/* acc[ii][jj] = sum_k dec(qa[i][k]) 2^ea[k/32][i] * dec(qb[j][k]) 2^eb[k/32][j],
+ * S[ii][jj] = the same sum of absolute values, binary64, i = rows[ii] (or ii),
+ * j = cols[jj] (or jj); K a multiple of 32. */
+void oracle_mx_gemm(int64_t K,
+                    const uint8_t* qa, int64_t lda, const int8_t* ea, int64_t ea_ld, int fmt_a,
+                    const uint8_t* qb, int64_t ldb, const int8_t* eb, int64_t eb_ld, int fmt_b,
+                    const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                    double* acc, double* S)
+{
+    build_tables();
+    const double* ta = g_table[fmt_a ? 1 : 0];
+    const double* tb = g_table[fmt_b ? 1 : 0];
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t ii = 0; ii < nrows; ++ii) {
+        const int64_t i = rows ? rows[ii] : ii;
+        for (int64_t jj = 0; jj < ncols; ++jj) {
+            const int64_t j = cols ? cols[jj] : jj;
+            double total = 0.0, total_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = ldexp(ta[qa[i * lda + k]], ea[(k / 32) * ea_ld + i]);
+                const double b = ldexp(tb[qb[j * ldb + k]], eb[(k / 32) * eb_ld + j]);
+                total += a * b;
+                total_abs += fabs(a * b);
+            }
+            acc[ii * ncols + jj] = total;
+            if (S) S[ii * ncols + jj] = total_abs;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* epilogue math ([P1]: bias, GELU, dGELU, db = column sum)                  */
 /* ------------------------------------------------------------------------ */
 

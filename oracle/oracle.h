@@ -46,6 +46,18 @@ void oracle_gemm(int64_t K, int64_t k0,
                  double* acc, double* S);
 
 /* epilogue math */
+/* MXFP8 (power-of-two scale per 32 elements, stored as the exponent e):
+ * quantize rows (transpose = 0: blocks along each row, q [rows][cols], e
+ * [cols/32][eld]) or columns (transpose = 1: blocks down each column, q
+ * [cols][rows], e [rows/32][eld]); GEMM over K (a multiple of 32). */
+void oracle_mx_quantize(int fmt, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                        int transpose, uint8_t* q, int8_t* e, int64_t eld);
+void oracle_mx_gemm(int64_t K,
+                    const uint8_t* qa, int64_t lda, const int8_t* ea, int64_t ea_ld, int fmt_a,
+                    const uint8_t* qb, int64_t ldb, const int8_t* eb, int64_t eb_ld, int fmt_b,
+                    const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
+                    double* acc, double* S);
+
 double oracle_gelu(double z);
 double oracle_dgelu(double z);
 void   oracle_gelu_array(const double* z, double* y, int64_t n);
