@@ -24,7 +24,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSP
 # every symbol include/fp8ll.h declares
 EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
            "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
-           "fp8_status_string", "fp8_debug_starve_next_gemm")
+           "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
+           "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad")
 
 
 class Fp8Error(RuntimeError):
@@ -36,6 +37,11 @@ class Fp8Error(RuntimeError):
 class OperandStruct(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("ld_q", ctypes.c_int64),
                 ("scale_ld", ctypes.c_int64), ("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class MxOperandStruct(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("ld_q", ctypes.c_int64), ("fmt", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -66,8 +72,16 @@ def lib():
         L.fp8_status_string.argtypes = [i32]
         L.fp8_status_string.restype = ctypes.c_char_p
         L.fp8_debug_starve_next_gemm.argtypes = [i32]
+        mop = ctypes.POINTER(MxOperandStruct)
+        L.fp8_mx_sf_bytes.argtypes = [i64, i64]
+        L.fp8_mx_sf_bytes.restype = sz
+        L.fp8_mx_quantize.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp]
+        L.fp8_mx_gemm_fprop.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp, vp, vp]
+        L.fp8_mx_gemm_dgrad.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp, vp, vp, sz, vp]
+        L.fp8_mx_gemm_wgrad.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp]
         for name in ("fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
-                     "fp8_gemm_wgrad",
+                     "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
+                     "fp8_mx_gemm_wgrad",
                      "fp8_grouped_wgrad", "fp8_get_device_status", "fp8_debug_starve_next_gemm"):
             getattr(L, name).restype = i32
         _lib = L
@@ -217,3 +231,94 @@ def device_status() -> int:
 
 def debug_starve_next_gemm(budget_ms: int):
     _check(lib().fp8_debug_starve_next_gemm(int(budget_ms)), "fp8_debug_starve_next_gemm")
+
+
+# ----------------------------------------------------------------- MXFP8 ----
+
+@dataclass
+class Fp8MxTensor:
+    """MXFP8 codes [rows][ld_q] (uint8) with UE8M0 scale bytes in the layout the
+    GEMM copies into tensor memory (see fp8ll.h)."""
+    q: torch.Tensor
+    sf: torch.Tensor
+    fmt: int
+
+    @property
+    def rows(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.q.shape[1]
+
+    def operand(self) -> MxOperandStruct:
+        return MxOperandStruct(self.q.data_ptr(), self.sf.data_ptr(), self.q.stride(0), int(self.fmt), 0)
+
+
+def mx_sf_bytes(rows: int, k: int) -> int:
+    return int(lib().fp8_mx_sf_bytes(int(rows), int(k)))
+
+
+def empty_mx(rows: int, k: int, fmt: int, device="cuda") -> Fp8MxTensor:
+    q = torch.empty((rows, k), dtype=torch.uint8, device=device)
+    sf = torch.empty((mx_sf_bytes(rows, k),), dtype=torch.uint8, device=device)
+    return Fp8MxTensor(q, sf, fmt)
+
+
+def mx_quantize(x: torch.Tensor, fmt: int, transpose: bool = False, out: Optional[Fp8MxTensor] = None) -> Fp8MxTensor:
+    """bf16 [rows][cols] -> Fp8MxTensor (one power-of-two scale per 32 elements).
+    transpose=False: blocks along rows, codes [rows][cols]; transpose=True:
+    blocks down columns, codes [cols][rows]."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if out is None:
+        out = empty_mx(cols, rows, fmt, x.device) if transpose else empty_mx(rows, cols, fmt, x.device)
+    _check(lib().fp8_mx_quantize(_ptr(x), rows, cols, x.stride(0), int(fmt), int(bool(transpose)), _ptr(out.q),
+                                 _ptr(out.sf), _stream()), "fp8_mx_quantize")
+    return out
+
+
+def mx_gemm_fprop(A: Fp8MxTensor, B: Fp8MxTensor, bias: Optional[torch.Tensor] = None, epi: int = EPI_BIAS_GELU,
+                  out: Optional[torch.Tensor] = None, aux: Optional[torch.Tensor] = None, want_aux: bool = True):
+    """Y (bf16 [M][N]) = epilogue(A B^T) with MX operands; returns (Y, Z-or-None)."""
+    M, N, K = A.rows, B.rows, A.k
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if aux is None and want_aux and epi == EPI_BIAS_GELU:
+        aux = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_mx_gemm_fprop(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(bias), int(epi), _ptr(out),
+                                   _ptr(aux), _stream()), "fp8_mx_gemm_fprop")
+    return out, aux
+
+
+def mx_gemm_dgrad(A: Fp8MxTensor, B: Fp8MxTensor, aux: torch.Tensor, epi: int = EPI_DGELU_BGRAD,
+                  out: Optional[torch.Tensor] = None, bgrad: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None):
+    """dZ (bf16 [M][N]) = (A B^T) * gelu'(aux) with MX operands (+ bias gradient [N])."""
+    M, N, K = A.rows, B.rows, A.k
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = 0
+    if epi == EPI_DGELU_BGRAD:
+        if bgrad is None:
+            bgrad = torch.empty((N,), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty((workspace_size(M, N) // 4,), dtype=torch.float32, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_mx_gemm_dgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(aux), int(epi), _ptr(out),
+                                   _ptr(bgrad), _ptr(workspace), ws_bytes, _stream()), "fp8_mx_gemm_dgrad")
+    return out, bgrad
+
+
+def mx_gemm_wgrad(A: Fp8MxTensor, B: Fp8MxTensor, out: torch.Tensor, accumulate: bool = True) -> torch.Tensor:
+    """fp32 out [M][N] (+)= A B^T with MX operands."""
+    M, N, K = A.rows, B.rows, A.k
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (M, N)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_mx_gemm_wgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(out), int(bool(accumulate)),
+                                   _stream()), "fp8_mx_gemm_wgrad")
+    return out

@@ -150,6 +150,66 @@ bool valid_mn(int64_t M, int64_t N) {
     return tiles < (1LL << 30) && M * N < (1LL << 46);
 }
 
+// TMA descriptor for MXFP8 codes [rows][kext] (row stride ld_q), 128 x box_rows
+// byte boxes with 128-byte swizzle; out-of-range rows read as zero.
+bool encode_codes(const uint8_t* q, int64_t ld_q, int64_t rows, int64_t kext, uint32_t box_rows, CUtensorMap* qmap) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kext), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_q)};
+    const cuuint32_t box[2] = {128, box_rows};
+    return enc(qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool valid_mx_operand(const fp8ll_mx_operand_t* op, int64_t rows, int64_t K) {
+    if (!op || !op->q || !op->sf || !valid_fmt(op->fmt)) return false;
+    if (!aligned16(op->q) || !aligned16(op->sf)) return false;
+    if (op->ld_q < K || op->ld_q % 16 != 0) return false;
+    if (rows < 1 || rows > (1LL << 31) - 1) return false;
+    return true;
+}
+
+// shared setup of the three MXFP8 GEMM entry points
+int mx_setup(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+             TensorMaps& maps, GemmParams& p, DeviceInfo** dev) {
+    if (!valid_mn(M, N) || K < 128 || K % 128 != 0 || K >= (1LL << 36)) return FP8LL_ERR_INVALID_ARG;
+    if (!valid_mx_operand(A, M, K) || !valid_mx_operand(B, N, K)) return FP8LL_ERR_INVALID_ARG;
+    int rc = current_device(dev);
+    if (rc != FP8LL_OK) return rc;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_codes(A->q, A->ld_q, M, K, 128, &maps.a) || !encode_codes(B->q, B->ld_q, N, K, kTileN, &maps.b))
+        return FP8LL_ERR_LAUNCH;
+    std::memset(&p, 0, sizeof(p));
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.num_m_tiles = static_cast<int32_t>((M + kTileM - 1) / kTileM);
+    p.num_n_tiles = static_cast<int32_t>((N + kTileN - 1) / kTileN);
+    p.tiles_per_group = p.num_m_tiles * p.num_n_tiles;
+    p.num_groups = 1;
+    p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
+    p.total_tiles = p.tiles_per_group;
+    // block-scaled instruction descriptor: formats, N >> 3, UE8M0 scales, M >> 4;
+    // the kernel adds the 32-element group id of each MMA for A and B
+    p.idesc = (static_cast<uint32_t>(A->fmt) << 7) | (static_cast<uint32_t>(B->fmt) << 10) |
+              ((static_cast<uint32_t>(kTileN) >> 3) << 17) | (1u << 23) | ((static_cast<uint32_t>(kTileM) >> 4) << 24);
+    p.status = (*dev)->status;
+    const int starve = g_starve_ms.exchange(0);
+    if (starve > 0) {
+        p.debug_starve = 1;
+        p.budget_ns = static_cast<uint64_t>(starve) * 1000000ull;
+    } else {
+        p.budget_ns = kDefaultBudgetNs;
+    }
+    p.sfa = A->sf;
+    p.sfb = B->sf;
+    p.sfa_groups = mx_sf_groups(M);
+    p.sfb_groups = mx_sf_groups(N);
+    return FP8LL_OK;
+}
+
 }  // namespace
 }  // namespace fp8ll
 
@@ -366,6 +426,99 @@ int fp8_debug_starve_next_gemm(int budget_ms) {
     if (budget_ms < 1 || budget_ms > 10000) return FP8LL_ERR_INVALID_ARG;
     g_starve_ms.store(budget_ms);
     return FP8LL_OK;
+}
+
+}  // extern "C"
+
+/* ------------------------------------------------------------------ MXFP8 */
+
+extern "C" {
+
+size_t fp8_mx_sf_bytes(int64_t rows, int64_t k) {
+    if (rows < 1 || k < 128 || k % 128 != 0) return 0;
+    return static_cast<size_t>(k / 128) * static_cast<size_t>(mx_sf_groups(rows)) * 512;
+}
+
+int fp8_mx_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                    uint8_t* sf, fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !valid_fmt(fmt) || (transpose != 0 && transpose != 1)) return FP8LL_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8LL_OK;
+    if (!x_bf16 || !q || !sf || !aligned16(x_bf16) || !aligned16(q) || !aligned16(sf)) return FP8LL_ERR_INVALID_ARG;
+    if (ldx < cols || ldx % 8 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (rows > (1LL << 31) - 1 || cols > (1LL << 31) - 1) return FP8LL_ERR_INVALID_ARG;
+    if (!transpose) {
+        if (cols % 128 != 0) return FP8LL_ERR_INVALID_ARG;
+    } else {
+        if (rows % 128 != 0 || cols % 8 != 0 || rows / 128 > 65535) return FP8LL_ERR_INVALID_ARG;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_mx_quantize(x_bf16, rows, cols, ldx, fmt, transpose, q, sf, reinterpret_cast<cudaStream_t>(stream),
+                              dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_mx_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+                      const void* bias_bf16, int epi, void* out_bf16, void* aux_bf16, fp8ll_stream_t stream) {
+    if (epi != FP8LL_EPI_NONE && epi != FP8LL_EPI_BIAS && epi != FP8LL_EPI_BIAS_GELU) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi != FP8LL_EPI_NONE && (!bias_bf16 || !aligned16(bias_bf16))) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    TensorMaps maps;
+    GemmParams p;
+    DeviceInfo* dev = nullptr;
+    int rc = mx_setup(M, N, K, A, B, maps, p, &dev);
+    if (rc != FP8LL_OK) return rc;
+    p.out = out_bf16;
+    p.aux = (epi == FP8LL_EPI_BIAS_GELU) ? aux_bf16 : nullptr;
+    p.bias = bias_bf16;
+    return launch_gemm_mx(maps, p, epi, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_mx_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+                      const void* aux_bf16, int epi, void* out_bf16, float* bgrad, void* workspace,
+                      size_t workspace_bytes, fp8ll_stream_t stream) {
+    if (epi != FP8LL_EPI_DGELU && epi != FP8LL_EPI_DGELU_BGRAD) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16) || !aux_bf16 || !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_DGELU_BGRAD) {
+        if (!bgrad || !aligned16(bgrad)) return FP8LL_ERR_INVALID_ARG;
+        if (!workspace || !aligned16(workspace) || workspace_bytes < fp8_workspace_size(M, N))
+            return FP8LL_ERR_WORKSPACE;
+    }
+    TensorMaps maps;
+    GemmParams p;
+    DeviceInfo* dev = nullptr;
+    int rc = mx_setup(M, N, K, A, B, maps, p, &dev);
+    if (rc != FP8LL_OK) return rc;
+    p.out = out_bf16;
+    p.aux = const_cast<void*>(aux_bf16);
+    p.workspace = static_cast<float*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_gemm_mx(maps, p, epi, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
+    if (epi == FP8LL_EPI_DGELU_BGRAD &&
+        launch_bgrad_finalize(static_cast<const float*>(workspace), static_cast<int64_t>(p.num_m_tiles) * 4, N, bgrad,
+                              s, dev->num_sms) != 0)
+        return FP8LL_ERR_LAUNCH;
+    return FP8LL_OK;
+}
+
+int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+                      float* out, int accumulate, fp8ll_stream_t stream) {
+    if (!out || !aligned16(out) || (accumulate != 0 && accumulate != 1)) return FP8LL_ERR_INVALID_ARG;
+    TensorMaps maps;
+    GemmParams p;
+    DeviceInfo* dev = nullptr;
+    int rc = mx_setup(M, N, K, A, B, maps, p, &dev);
+    if (rc != FP8LL_OK) return rc;
+    p.out = out;
+    p.accumulate = accumulate;
+    return launch_gemm_mx(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
 }
 
 }  // extern "C"

@@ -43,6 +43,10 @@ struct GemmParams {
     const void* bias;     // bf16 [N]
     float* workspace;     // fp32 [4 * num_m_tiles][N] bias-gradient partials (one per 32-row band)
     int* status;          // device status word
+    const uint8_t* sfa;   // MXFP8: scale atoms of A and B (UE8M0, the MX cast's layout)
+    const uint8_t* sfb;
+    int64_t sfa_groups;   // MXFP8: 128-row groups per K block of each scale array
+    int64_t sfb_groups;
     GroupEntry groups[kMaxGroups];
 };
 
@@ -52,6 +56,9 @@ struct TensorMaps {
 
 int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
                     float* scale, int64_t sld, cudaStream_t stream, int num_sms);
+int64_t mx_sf_groups(int64_t rows);
+int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                       uint8_t* sf, cudaStream_t stream, int num_sms);
 int launch_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, cudaStream_t stream, int num_sms);
 
 // GEMM launchers, one per epilogue family (separate translation units).
@@ -60,6 +67,7 @@ int launch_gemm_fprop(const TensorMaps& maps, const GemmParams& p, int epi, int 
 int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, int fast, cudaStream_t stream,
                       int grid);
 int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, int fast, cudaStream_t stream, int grid);
+int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* bgrad, cudaStream_t stream,
                           int num_sms);
 size_t gemm_smem_bytes();

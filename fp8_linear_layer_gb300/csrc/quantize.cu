@@ -211,6 +211,150 @@ __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* _
     }
 }
 
+// -------------------------------------------------------------------- MXFP8
+// One power-of-two scale per 32 consecutive elements (the MX block format),
+// e = the smallest integer in [-127, 127] with amax <= FMAX 2^e (no element
+// saturates; 0 for an all-zero block), codes = fp8(x 2^-e) with a single
+// rounding (scaling by a power of two is exact).  The scale bytes (UE8M0,
+// e + 127) are written in the layout the GEMM copies into tensor memory:
+// 512-byte atoms per (128-element K block kb, 128-row group g), row
+// r = 128 g + rr and 32-element group k of the block at byte
+//   (kb * G + g) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + k,
+// G = 2 * ceil(rows / 256) (an even number of groups, so that the two atoms of
+// a 256-row tile are adjacent).  Bytes of rows beyond the matrix are 127.
+
+template <int FMT>
+__device__ __forceinline__ int mx_exponent(float amax) {
+    // FMAX = 1.75 * 2^F; amax = (1 + m) 2^(E - 127) <= 1.75 2^(F + e)
+    //   <=> e >= E - 127 - F + (m > 0.75)
+    constexpr int F = (FMT == 0) ? 8 : 15;
+    const uint32_t b = __float_as_uint(amax);
+    if (b == 0u) return 0;
+    const int E = static_cast<int>(b >> 23);
+    if (E == 0) return -127;  // subnormal amax: far below FMAX 2^-127
+    int e = E - 127 - F + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    e = e < -127 ? -127 : e;
+    return e > 127 ? 127 : e;
+}
+
+// 2^-e as an fp32 (2^-127 is subnormal)
+__device__ __forceinline__ float mx_inverse_scale(int e) {
+    return e < 127 ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : __uint_as_float(0x400000u);
+}
+
+__device__ __forceinline__ int64_t mx_sf_offset(int64_t kb, int64_t groups, int64_t r, int k) {
+    const int64_t rr = r & 127;
+    return (kb * groups + (r >> 7)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + k;
+}
+
+// Rows: a half-warp per (row, 128-block) task as in the 1x128 cast; lane l of
+// the half holds elements 8l..8l+7, so lanes 4k..4k+3 form MX group k.
+template <int FMT, int U>
+__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                               int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
+                                                               uint8_t* __restrict__ sf, int64_t groups) {
+    const int64_t nb = cols / 128;
+    const int64_t total = rows * nb;
+    const int lane = threadIdx.x & 31;
+    const int hl = lane & 15;
+    const int hw = lane >> 4;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t base = warp * 2 * U; base < total; base += nwarps * 2 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t task = base + 2 * u + hw;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (task < total) {
+                const int64_t r = task / nb;
+                v[u] = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + (task - r * nb) * 128 + hl * 8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t task = base + 2 * u + hw;
+            float f[8];
+            f[0] = bf16_lo(v[u].x); f[1] = bf16_hi(v[u].x);
+            f[2] = bf16_lo(v[u].y); f[3] = bf16_hi(v[u].y);
+            f[4] = bf16_lo(v[u].z); f[5] = bf16_hi(v[u].z);
+            f[6] = bf16_lo(v[u].w); f[7] = bf16_hi(v[u].w);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int e = mx_exponent<FMT>(amax);
+            const uint2 codes = encode8<FMT>(f, mx_inverse_scale(e));
+            if (task < total) {
+                const int64_t r = task / nb;
+                const int64_t b = task - r * nb;
+                *reinterpret_cast<uint2*>(q + r * cols + b * 128 + hl * 8) = codes;
+                if ((hl & 3) == 0) sf[mx_sf_offset(b, groups, r, hl >> 2)] = static_cast<uint8_t>(e + 127);
+            }
+        }
+    }
+}
+
+// Transposed: the 1x128 kernel's staged 128 x 128 tile; a thread's 32 rows of
+// a column are exactly one MX group (group p of the 128-token block).
+template <int FMT>
+__global__ void __launch_bounds__(256, 4) mx_quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                  int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
+                                                                  uint8_t* __restrict__ sf, int64_t groups) {
+    __shared__ __align__(16) uint32_t tile[128][64];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int i = threadIdx.x + it * 256;
+        const int rr = i >> 4;
+        const int ch = i & 15;
+        const int64_t c = c0 + ch * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (c < cols) v = __ldcs(reinterpret_cast<const uint4*>(x + (r0 + rr) * ldx + c));
+        const int w = (ch * 4 + 8 * (rr >> 5)) & 63;
+        *reinterpret_cast<uint4*>(&tile[rr][w]) = v;
+    }
+    __syncthreads();
+    const int cp = threadIdx.x >> 2;
+    const int p = threadIdx.x & 3;
+    const int64_t c = c0 + 2 * cp;
+    float amax_lo = 0.0f, amax_hi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
+        amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
+        amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
+    }
+    const int e_lo = mx_exponent<FMT>(amax_lo), e_hi = mx_exponent<FMT>(amax_hi);
+    const float inv_lo = mx_inverse_scale(e_lo), inv_hi = mx_inverse_scale(e_hi);
+    if (c < cols) {
+        uint32_t wl[8], wh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t lo16[2], hi16[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t w0 = tile[32 * p + 4 * i + 2 * k][(cp + 8 * p) & 63];
+                const uint32_t w1 = tile[32 * p + 4 * i + 2 * k + 1][(cp + 8 * p) & 63];
+                lo16[k] = Fp8Fmt<FMT>::cvt2(__fmul_rn(bf16_lo(w0), inv_lo), __fmul_rn(bf16_lo(w1), inv_lo));
+                hi16[k] = Fp8Fmt<FMT>::cvt2(__fmul_rn(bf16_hi(w0), inv_hi), __fmul_rn(bf16_hi(w1), inv_hi));
+            }
+            wl[i] = lo16[0] | (lo16[1] << 16);
+            wh[i] = hi16[0] | (hi16[1] << 16);
+        }
+        uint4* dl = reinterpret_cast<uint4*>(q + c * rows + r0 + 32 * p);
+        uint4* dh = reinterpret_cast<uint4*>(q + (c + 1) * rows + r0 + 32 * p);
+        dl[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+        dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+        sf[mx_sf_offset(blockIdx.y, groups, c, p)] = static_cast<uint8_t>(e_lo + 127);
+        sf[mx_sf_offset(blockIdx.y, groups, c + 1, p)] = static_cast<uint8_t>(e_hi + 127);
+    }
+}
+
 // ---------------------------------------------------------------- plain cast
 template <int FMT>
 __global__ void cast_f32_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ q) {
@@ -259,6 +403,42 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
             quantize_cols_kernel<0><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
         else
             quantize_cols_kernel<1><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int64_t mx_sf_groups(int64_t rows) { return 2 * ((rows + 255) / 256); }
+
+int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                       uint8_t* sf, cudaStream_t stream, int num_sms) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    // rows of the quantized operand and its K extent
+    const int64_t orows = transpose ? cols : rows;
+    const int64_t kext = transpose ? rows : cols;
+    const int64_t groups = mx_sf_groups(orows);
+    if (orows % 256 != 0) {
+        // rows beyond the matrix in the last group pair read as scale 1
+        if (cudaMemsetAsync(sf, 127, static_cast<size_t>(kext / 128) * groups * 512, stream) != cudaSuccess)
+            return -3;
+    }
+    if (!transpose) {
+        constexpr int U = 4;
+        const int64_t total = rows * (cols / 128);
+        int64_t blocks = ((total + 1) / 2 + 8 * U - 1) / (8 * U);
+        const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        const unsigned g = static_cast<unsigned>(blocks);
+        if (fmt == 0)
+            mx_quantize_rows_kernel<0, U><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+        else
+            mx_quantize_rows_kernel<1, U><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+    } else {
+        dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+        if (fmt == 0)
+            mx_quantize_cols_kernel<0><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+        else
+            mx_quantize_cols_kernel<1><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

@@ -197,6 +197,59 @@ int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
 int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const fp8ll_operand_t* A,
                       const fp8ll_operand_t* B, float* out, int accumulate, int acc_mode, fp8ll_stream_t stream);
 
+/* ------------------------------------------------------------------ MXFP8
+ * The MX block format, named among the fp8 recipes on "How can we use
+ * te.Linear with weight parallel?": one power-of-two scale per 32 consecutive
+ * K-elements of every operand row, applied by the tensor core itself
+ * (block-scaled MMA), so the fp32 accumulation runs over the whole K range
+ * with no software promotion.  Scale of a block: 2^e with e the smallest
+ * integer in [-127, 127] such that amax <= FMAX * 2^e (no element saturates;
+ * e = 0 for an all-zero block); codes: round-to-nearest-even, saturating fp8
+ * of x * 2^-e.
+ *
+ * Scale storage (UE8M0 bytes, e + 127), the layout the GEMM copies into
+ * tensor memory unchanged: for an operand with `rows` rows and K columns,
+ * G = 2 * ceil(rows / 256) groups of 128 rows; K block kb (128 elements),
+ * row r = 128 * g + rr, 32-element group k in 0..3 of the block:
+ *   sf[(kb * G + g) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + k]
+ * Bytes of rows beyond the operand hold 127 (scale 1). */
+typedef struct {
+    const uint8_t* q;  /* codes [rows][ld_q], K contiguous; 16-byte aligned */
+    const uint8_t* sf; /* scale bytes, fp8_mx_sf_bytes(rows, K) of them; 16-byte aligned */
+    int64_t ld_q;      /* >= K, multiple of 16 */
+    int32_t fmt;
+    int32_t reserved;
+} fp8ll_mx_operand_t;
+
+/* Bytes of scale storage for an operand of `rows` rows and `k` columns
+ * (k % 128 == 0); 0 for invalid sizes. */
+size_t fp8_mx_sf_bytes(int64_t rows, int64_t k);
+
+/* MXFP8 cast of a bf16 matrix x [rows][cols] (row stride ldx elements,
+ * ldx % 8 == 0).  transpose = 0: blocks along each row, q [rows][cols],
+ * cols % 128 == 0, sf for (rows, cols).  transpose = 1: blocks down each
+ * column, q [cols][rows] (the transpose), rows % 128 == 0, cols % 8 == 0, sf
+ * for (cols, rows).  Codes and scales are bit-exact against the definition
+ * above.  Caller-owned device buffers; asynchronous on `stream`. */
+int fp8_mx_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
+                    uint8_t* sf, fp8ll_stream_t stream);
+
+/* MXFP8 GEMMs: the three GEMMs above with MX operands, the same epilogues,
+ * shapes, layouts and error codes (no accumulation mode: the tensor core
+ * applies every block's scales):
+ *   fp8_mx_gemm_fprop: out = epi(A . B^T + bias), epi NONE / BIAS / BIAS_GELU
+ *   fp8_mx_gemm_dgrad: out = (A . B^T) * gelu'(aux), bias gradient as in
+ *                      fp8_gemm_dgrad (same workspace size)
+ *   fp8_mx_gemm_wgrad: out (+)= A . B^T, fp32
+ * K % 128 == 0; M, N >= 1. */
+int fp8_mx_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+                      const void* bias_bf16, int epi, void* out_bf16, void* aux_bf16, fp8ll_stream_t stream);
+int fp8_mx_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+                      const void* aux_bf16, int epi, void* out_bf16, float* bgrad, void* workspace,
+                      size_t workspace_bytes, fp8ll_stream_t stream);
+int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
+                      float* out, int accumulate, fp8ll_stream_t stream);
+
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: FP8LL_OK, or the first FP8LL_ERR_TIMEOUT recorded by a
  * kernel since the last call; FP8LL_ERR_LAUNCH if CUDA reports an error. */

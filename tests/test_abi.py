@@ -82,3 +82,28 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.fp8_grouped_wgrad(0, 8, 8, ks0, ob, ob, fake, 1, 0, None) == E
     assert L.fp8_grouped_wgrad(1, 8, 8, ks0, ob, ob, fake, 2, 0, None) == E             # accumulate flag
     assert L.fp8_debug_starve_next_gemm(0) == E
+
+
+def test_mx_sizes_and_validation(L):
+    import fp8_linear_layer_gb300 as f
+    # groups of 128 rows, rounded up to an even count, 512 bytes per group and K block
+    assert f.mx_sf_bytes(256, 128) == 2 * 512
+    assert f.mx_sf_bytes(300, 4096) == 32 * 4 * 512
+    assert f.mx_sf_bytes(1, 256) == 2 * 2 * 512
+    assert f.mx_sf_bytes(0, 128) == 0 and f.mx_sf_bytes(128, 100) == 0
+    E = f.binding.ERR_INVALID_ARG
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    # rows cast needs cols % 128 == 0; transposed needs rows % 128 == 0
+    assert L.fp8_mx_quantize(fake, 4, 100, 104, 0, 0, fake, fake, None) == E
+    assert L.fp8_mx_quantize(fake, 100, 64, 64, 0, 1, fake, fake, None) == E
+    assert L.fp8_mx_quantize(fake, 4, 128, 128, 7, 0, fake, fake, None) == E
+    op = f.binding.MxOperandStruct(0x10000, 0x10000, 256, 0, 0)
+    bad = f.binding.MxOperandStruct(0x10000, 0x10008, 256, 0, 0)  # misaligned scales
+    out = vp(0x20000)
+    assert L.fp8_mx_gemm_wgrad(128, 128, 100, ctypes.byref(op), ctypes.byref(op), out, 1, None) == E
+    assert L.fp8_mx_gemm_wgrad(128, 128, 256, ctypes.byref(bad), ctypes.byref(op), out, 1, None) == E
+    assert L.fp8_mx_gemm_fprop(128, 128, 256, ctypes.byref(op), ctypes.byref(op), None, 9, out, None, None) == E
+    assert L.fp8_mx_gemm_dgrad(128, 128, 256, ctypes.byref(op), ctypes.byref(op), None, 4, out, None, None, 0,
+                               None) == E
+
