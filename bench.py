@@ -74,12 +74,15 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--acc", choices=["full", "fast"], default="full")
+    ap.add_argument("--recipe", choices=["block128", "mx"], default="block128",
+                    help="block128: one fp32 scale per 128 elements, promoted in software (the configured "
+                         "workload); mx: MXFP8, one power-of-two scale per 32 elements applied by the tensor core")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables"], default=None,
+    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx"], default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
     ap.add_argument("--study-k", type=int, default=16384)
@@ -343,7 +346,11 @@ def run_ours(args):
     default_size = (m, k, n) == (M_TOK, K_IN, N_OUT)
     hX, hW, hb, hdY = inputs(dev, m, k, n)
     X, W, b, dY = (t.to(dev, non_blocking=True) for t in (hX, hW, hb, hdY))
-    step = LinearTrainStep(m, k, n, dev, acc_mode)
+    if args.recipe == "mx":
+        from fp8_linear_layer_gb300.linear import MxLinearTrainStep
+        step = MxLinearTrainStep(m, k, n, dev)
+    else:
+        step = LinearTrainStep(m, k, n, dev, acc_mode)
     launches = step.launches(X, W, b, dY)
     stream = torch.cuda.current_stream()
 
@@ -401,7 +408,7 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = run_e2e(args, step, (hX, hW, hb, hdY), (X, W, b, dY), stream, barrier, world, dev)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and default_size:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and default_size and args.recipe == "block128":
         v, dt, cores, sample = cpu_baseline_sample()
         cpu = {"value": v, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
@@ -411,15 +418,19 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8(e4m3/e5m2) x fp8 -> fp32 accumulate", "data": "synthetic",
-            "config": {"workload": WORKLOAD if default_size else "linear_train_step_m%d_k%d_n%d_bias_gelu" % (m, k, n),
+            "config": {"workload": (WORKLOAD if default_size else "linear_train_step_m%d_k%d_n%d_bias_gelu" % (m, k, n))
+                       + ("_mxfp8" if args.recipe == "mx" else ""),
                        "m_tokens": m, "k_in": k, "n_out": n,
-                       "acc_mode": args.acc, "parallelism": "replicas" if world > 1 else "single",
+                       "acc_mode": args.acc if args.recipe == "block128" else None, "recipe": args.recipe,
+                       "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
-            "roofline": {"bound": "tensor", "kernel": "gemm_fp8_kernel (fprop, dgrad, wgrad launches)",
+            "roofline": {"bound": "tensor", "kernel": ("gemm_mx_kernel" if args.recipe == "mx" else "gemm_fp8_kernel")
+                         + " (fprop, dgrad, wgrad launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),
-                         "traffic": measured_traffic() if default_size else None, "traffic_unit": "bytes",
+                         "traffic": measured_traffic() if default_size and args.recipe == "block128" else None,
+                         "traffic_unit": "bytes",
                          "avg_gemm_ms": avg_gemm_ms},
             "e2e": e2e,
             "gpu_launches": step.KERNELS_PER_STEP * args.steps,
@@ -604,6 +615,68 @@ def run_wgrad_tables(args):
                       "status": fp8.device_status()}))
 
 
+def run_mx_study(args):
+    """The MXFP8 GEMMs (tensor-core block scaling, no software promotion) at the
+    training-step shapes and on long K, next to the 1x128 GEMMs on the same
+    bf16 data: CUDA events around 10 launches after 3 warm-ups, TFLOP/s;
+    plus the MX casts in GB/s of algorithmic bytes (2 read + 1 + 1/32 written
+    per element)."""
+    import torch
+    import workloads
+    import fp8_linear_layer_gb300 as fp8
+    reps = 10
+    m, k, n = args.m, args.k, args.n
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps
+
+    res = {"study": "mx", "reps": reps, "mx_tflops": {}, "block128_tflops": {}, "mx_cast_gbs": {}}
+    x = workloads.normal_bf16((m, k), SEED, "X").cuda()
+    w = workloads.normal_bf16((n, k), SEED, "W", std=0.02).cuda()
+    bias = workloads.normal_bf16((n,), SEED, "b", std=0.02).cuda()
+    dy = workloads.normal_bf16((m, k), SEED, "dY", std=1e-2).cuda()
+    f = 2.0 * m * n * k / 1e9
+    Y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    Z, dZ = torch.empty_like(Y), torch.empty_like(Y)
+    X, W, DY = fp8.mx_quantize(x, fp8.E4M3), fp8.mx_quantize(w, fp8.E4M3), fp8.mx_quantize(dy, fp8.E5M2)
+    res["mx_tflops"]["fprop_bias_gelu_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.mx_gemm_fprop(X, W, bias, fp8.EPI_BIAS_GELU, out=Y, aux=Z))
+    res["mx_tflops"]["dgrad_dgelu_bgrad_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.mx_gemm_dgrad(DY, W, Z, fp8.EPI_DGELU_BGRAD, out=dZ))
+    DZT, XT = fp8.mx_quantize(dZ, fp8.E5M2, transpose=True), fp8.mx_quantize(x, fp8.E4M3, transpose=True)
+    dW = torch.zeros((n, k), device="cuda")
+    res["mx_tflops"]["wgrad_accumulate_m%d_n%d_k%d" % (n, k, m)] = f / timed(lambda: fp8.mx_gemm_wgrad(DZT, XT, dW))
+    del X, W, DY, DZT, XT
+    a = workloads.normal_bf16((8192, 16384), SEED + 1, "A", std=0.02).cuda()
+    bb = workloads.normal_bf16((8192, 16384), SEED + 1, "B", std=0.02).cuda()
+    fl = 2.0 * 8192 * 8192 * 16384 / 1e9
+    o = torch.zeros((8192, 8192), device="cuda")
+    Am, Bm = fp8.mx_quantize(a, fp8.E4M3), fp8.mx_quantize(bb, fp8.E4M3)
+    res["mx_tflops"]["wgrad_accumulate_m8192_n8192_k16384"] = fl / timed(lambda: fp8.mx_gemm_wgrad(Am, Bm, o))
+    del Am, Bm
+    Ab, Bb = fp8.quantize(a, fp8.E4M3), fp8.quantize(bb, fp8.E4M3)
+    res["block128_tflops"]["wgrad_accumulate_m8192_n8192_k16384"] = fl / timed(lambda: fp8.gemm_wgrad(Ab, Bb, o))
+    del Ab, Bb
+    xb = workloads.normal_bf16((32768, 8192), SEED + 2, "C").cuda()
+    gb = xb.numel() * (3.0 + 1.0 / 32) / 1e6
+    out_r = fp8.empty_mx(32768, 8192, fp8.E4M3, xb.device)
+    out_t = fp8.empty_mx(8192, 32768, fp8.E4M3, xb.device)
+    res["mx_cast_gbs"]["rows_e4m3_32768x8192"] = gb / timed(lambda: fp8.mx_quantize(xb, fp8.E4M3, out=out_r))
+    res["mx_cast_gbs"]["transposed_e4m3_32768x8192"] = gb / timed(
+        lambda: fp8.mx_quantize(xb, fp8.E4M3, transpose=True, out=out_t))
+    res["status"] = fp8.device_status()
+    print(json.dumps(res))
+
+
 def run_fp8_peak_probe(args):
     """Dense fp8 tensor-core throughput of the vendor library on this GPU, for
     context beside the roofline denominator (which stays the measured bf16
@@ -663,6 +736,8 @@ def main():
         return run_fp8_peak_probe(args)
     if args.study == "wgrad_tables":
         return run_wgrad_tables(args)
+    if args.study == "mx":
+        return run_mx_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -249,7 +249,7 @@ __device__ __forceinline__ int64_t mx_sf_offset(int64_t kb, int64_t groups, int6
 
 // Rows: a half-warp per (row, 128-block) task as in the 1x128 cast; lane l of
 // the half holds elements 8l..8l+7, so lanes 4k..4k+3 form MX group k.
-template <int FMT, int U>
+template <int FMT, int U, bool PACKED>
 __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
                                                                uint8_t* __restrict__ sf, int64_t groups) {
@@ -267,8 +267,14 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* _
             const int64_t task = base + 2 * u + hw;
             v[u] = make_uint4(0, 0, 0, 0);
             if (task < total) {
-                const int64_t r = task / nb;
-                v[u] = __ldcs(reinterpret_cast<const uint4*>(x + r * ldx + (task - r * nb) * 128 + hl * 8));
+                const uint16_t* src;
+                if (PACKED) {
+                    src = x + task * 128 + hl * 8;
+                } else {
+                    const int64_t r = task / nb;
+                    src = x + r * ldx + (task - r * nb) * 128 + hl * 8;
+                }
+                v[u] = __ldcs(reinterpret_cast<const uint4*>(src));
             }
         }
 #pragma unroll
@@ -287,10 +293,20 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* _
             const int e = mx_exponent<FMT>(amax);
             const uint2 codes = encode8<FMT>(f, mx_inverse_scale(e));
             if (task < total) {
-                const int64_t r = task / nb;
-                const int64_t b = task - r * nb;
-                *reinterpret_cast<uint2*>(q + r * cols + b * 128 + hl * 8) = codes;
-                if ((hl & 3) == 0) sf[mx_sf_offset(b, groups, r, hl >> 2)] = static_cast<uint8_t>(e + 127);
+                *reinterpret_cast<uint2*>(q + task * 128 + hl * 8) = codes;
+                if ((hl & 3) == 0) {
+                    int64_t r, b;
+                    if (total <= 0xFFFFFFFFll) {
+                        const uint32_t t32 = static_cast<uint32_t>(task), nb32 = static_cast<uint32_t>(nb);
+                        const uint32_t r32 = t32 / nb32;
+                        r = r32;
+                        b = t32 - r32 * nb32;
+                    } else {
+                        r = task / nb;
+                        b = task - r * nb;
+                    }
+                    sf[mx_sf_offset(b, groups, r, hl >> 2)] = static_cast<uint8_t>(e + 127);
+                }
             }
         }
     }
@@ -429,10 +445,18 @@ int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, i
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
         const unsigned g = static_cast<unsigned>(blocks);
-        if (fmt == 0)
-            mx_quantize_rows_kernel<0, U><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
-        else
-            mx_quantize_rows_kernel<1, U><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+        const bool packed = ldx == cols;
+        if (fmt == 0) {
+            if (packed)
+                mx_quantize_rows_kernel<0, U, true><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+            else
+                mx_quantize_rows_kernel<0, U, false><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+        } else {
+            if (packed)
+                mx_quantize_rows_kernel<1, U, true><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+            else
+                mx_quantize_rows_kernel<1, U, false><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
+        }
     } else {
         dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
         if (fmt == 0)

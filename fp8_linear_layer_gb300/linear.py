@@ -102,3 +102,58 @@ class LinearTrainStep:
 
     # 5 quantize + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
     KERNELS_PER_STEP = 9
+
+
+class MxLinearTrainStep(LinearTrainStep):
+    """The same training step on MXFP8 operands: every cast puts one
+    power-of-two scale on each 32 elements and every GEMM lets the tensor core
+    apply them (no software promotion).  Same buffers for the outputs, the
+    same 9 launches per step."""
+
+    def __init__(self, m: int, k: int, n: int, device="cuda"):
+        assert m % 128 == 0 and k % 128 == 0
+        self.m, self.k, self.n = m, k, n
+        self.acc_mode = B.ACC_FULL
+        dev = torch.device(device)
+        self.Xq = B.empty_mx(m, k, B.E4M3, dev)
+        self.Wq = B.empty_mx(n, k, B.E4M3, dev)
+        self.dYq = B.empty_mx(m, k, B.E5M2, dev)
+        self.dZTq = B.empty_mx(n, m, B.E5M2, dev)
+        self.XTq = B.empty_mx(k, m, B.E4M3, dev)
+        self.Y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.Z = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.dZ = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.db = torch.empty((n,), dtype=torch.float32, device=dev)
+        self.dW = torch.zeros((n, k), dtype=torch.float32, device=dev)
+        self.ws = torch.empty((B.workspace_size(m, n) // 4,), dtype=torch.float32, device=dev)
+
+    def forward(self, X, W, b):
+        B.mx_quantize(X, B.E4M3, out=self.Xq)
+        B.mx_quantize(W, B.E4M3, out=self.Wq)
+        B.mx_gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, out=self.Y, aux=self.Z)
+        return self.Y
+
+    def backward(self, X, dY):
+        B.mx_quantize(dY, B.E5M2, out=self.dYq)
+        B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ, bgrad=self.db, workspace=self.ws)
+        B.mx_quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)
+        B.mx_quantize(X, B.E4M3, transpose=True, out=self.XTq)
+        B.mx_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True)
+        return self.dW, self.db
+
+    def input_grad(self, W):
+        raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+
+    def launches(self, X, W, b, dY):
+        return [
+            ("quantize", lambda: B.mx_quantize(X, B.E4M3, out=self.Xq)),
+            ("quantize", lambda: B.mx_quantize(W, B.E4M3, out=self.Wq)),
+            ("gemm", lambda: B.mx_gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, out=self.Y, aux=self.Z)),
+            ("quantize", lambda: B.mx_quantize(dY, B.E5M2, out=self.dYq)),
+            ("gemm", lambda: B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ,
+                                             bgrad=self.db, workspace=self.ws)),
+            ("quantize", lambda: B.mx_quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)),
+            ("quantize", lambda: B.mx_quantize(X, B.E4M3, transpose=True, out=self.XTq)),
+            ("gemm", lambda: B.mx_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True)),
+        ]
+
