@@ -128,6 +128,9 @@ void init_params(GemmParams& p, int64_t M, int64_t N, const fp8ll_operand_t* A, 
     p.num_m_tiles = static_cast<int32_t>((M + kTileM - 1) / kTileM);
     p.num_n_tiles = static_cast<int32_t>((N + kTileN - 1) / kTileN);
     p.tiles_per_group = p.num_m_tiles * p.num_n_tiles;
+    // instruction descriptor of kind::f8f6f4 (fmt 0 = e4m3, 1 = e5m2): bits 4-5
+    // D format (1 = f32), 7-9 A format, 10-12 B format, 15/16 A/B major (0 = K),
+    // 17-22 N >> 3, 24-28 M >> 4
     p.idesc = (1u << 4) | (static_cast<uint32_t>(A->fmt) << 7) | (static_cast<uint32_t>(B->fmt) << 10) |
               ((static_cast<uint32_t>(kTileN) >> 3) << 17) | ((static_cast<uint32_t>(kTileM) >> 4) << 24);
     p.status = dev->status;
@@ -142,6 +145,22 @@ void init_params(GemmParams& p, int64_t M, int64_t N, const fp8ll_operand_t* A, 
 
 int grid_for(const GemmParams& p, const DeviceInfo* dev) {
     return p.total_tiles < dev->num_sms ? p.total_tiles : dev->num_sms;
+}
+
+// TMA descriptor for the stored pre-activation Z (bf16 [M][N], row stride
+// N * 2 bytes, which TMA needs to be a multiple of 16: N % 8 == 0) in boxes
+// of 64 columns x 128 rows with 128-byte swizzling; outside the matrix reads
+// as zero.
+bool encode_z(const void* z, int64_t M, int64_t N, CUtensorMap* zmap) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileM)};
+    return enc(zmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(z), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool valid_mn(int64_t M, int64_t N) {
@@ -315,6 +334,13 @@ int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     p.out = out_bf16;
     p.aux = const_cast<void*>(aux_bf16);
     p.workspace = static_cast<float*>(workspace);
+    // Z tiles go through shared memory by TMA when its rows are 16-byte aligned;
+    // otherwise the epilogue reads them from global memory
+    std::memset(&maps.z, 0, sizeof(maps.z));
+    if (N % 8 == 0) {
+        if (!encode_z(aux_bf16, M, N, &maps.z)) return FP8LL_ERR_LAUNCH;
+        p.z_tma = 1;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_gemm_dgrad(maps, p, epi, acc_mode, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
     if (epi == FP8LL_EPI_DGELU_BGRAD) {

@@ -20,6 +20,4 @@ int launch_gemm_fprop(const TensorMaps& maps, const GemmParams& p, int epi, int 
     }
 }
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
-
 }  // namespace fp8ll

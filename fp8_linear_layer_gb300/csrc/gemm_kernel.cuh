@@ -11,15 +11,20 @@
 // CTA = 3 warpgroups (12 warps), one CTA per SM, persistent over a
 // rasterized tile list of 128 x 256 output tiles:
 //   warp 0      TMA producer: operand tiles (128 x 128 B of A, 256 x 128 B of
-//               B, 128-byte swizzle) into a 4-stage ring, block scales into
-//               an 8-stage ring.
+//               B, 128-byte swizzle) into a 3-stage ring, block scales into
+//               an 8-stage ring (more operand stages measured slower).
 //   warp 1      TMEM owner and MMA issuer: per K block, 4 x tcgen05.mma
 //               (M=128, N=256, K=32, kind::f8f6f4) into one of two TMEM
 //               accumulators (2 x 256 fp32 columns), so the MMAs of block
 //               k+1 run while block k is promoted.  An N=256 MMA does twice
 //               the work of an N=128 one for the same A operand read, and
 //               the tensor core only reaches its full rate at this width.
-//   warps 2-3   idle (they complete the first warpgroup).
+//   warp 2      dgrad only: TMA loader of the stored pre-activation tile Z
+//               (128 x 256 bf16, four 64-column boxes, 128-byte swizzle) into
+//               a one-slot shared-memory buffer, issued as soon as the previous
+//               tile's epilogue has released it, so that it lands during the
+//               K loop instead of being fetched by the epilogue.
+//   warp 3      idle (completes the first warpgroup).
 //   warps 4-11  promotion + epilogue, two warpgroups of 128 columns each:
 //               warp w reads TMEM lanes 32*(w%4)..+31 (its rows) in the
 //               16x256b fragment shape, so a thread holds four rows x two
@@ -51,7 +56,7 @@ namespace fp8ll {
 constexpr int kBM = kTileM;
 constexpr int kBN = kTileN;
 constexpr int kBK = 128;  // K bytes per stage == one scale block
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kSStages = 8;
 constexpr int kEpiGroups = 2;               // epilogue warpgroups
 constexpr int kEpiWarps = 4 * kEpiGroups;
@@ -80,11 +85,26 @@ struct __align__(1024) SmemLayout {
     uint64_t sempty[kSStages];
     uint64_t acc_full[kNumAcc];
     uint64_t acc_empty[kNumAcc];
+    uint64_t zfull, zempty;
     uint64_t drain;
     uint32_t tmem_base;
 };
-constexpr size_t kSmemBytes = sizeof(SmemLayout) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+// The dgrad kernels add the Z tile buffer right after the layout (1024-byte
+// aligned, as 128-byte swizzling needs): four boxes of 128 rows x 64 columns.
+constexpr int kZBoxCols = 64;
+constexpr uint32_t kZBoxBytes = kBM * kZBoxCols * 2;
+constexpr uint32_t kZBytes = kBM * kBN * 2;
+static_assert(sizeof(SmemLayout) % 1024 == 0, "Z buffer alignment");
+
+template <int EPI>
+constexpr bool uses_z() {
+    return EPI == kEpiDgelu || EPI == kEpiDgeluBgrad;
+}
+template <int EPI>
+constexpr size_t smem_bytes() {
+    return sizeof(SmemLayout) + (uses_z<EPI>() ? kZBytes : 0) + 1024;
+}
+static_assert(smem_bytes<kEpiDgelu>() <= 232448, "shared memory budget");
 
 template <int N>
 __device__ __forceinline__ void ring_advance(int& idx, uint32_t& phase) {
@@ -220,9 +240,18 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int c
 // thread's four rows first, then across the eight lanes that hold the same
 // columns (lane xor 4, 8, 16), a fixed order, so results are deterministic --
 // and lanes 0..3 write the chunk's eight sums to the workspace band of this warp.
-// The stored pre-activations are read one chunk (4 bf16 pairs) at a time,
-// the next chunk's loads in flight while the current one is computed.
+//
+// The stored pre-activations come from one of two places.  ZSMEM: the tile's
+// Z was staged in shared memory by TMA (zs = the 128 x 256 tile as four
+// 64-column boxes with 128-byte swizzling; zeros outside the matrix).  Row r
+// of a box is 128 bytes at r * 128, and its 16-byte chunk j sits at
+// (j ^ (r % 8)) * 16: the eight rows and four column pairs that one load
+// instruction of a warp touches fall in 32 distinct banks.  Otherwise (rows
+// of Z not 16-byte aligned) Z is read from global memory one chunk (4 bf16
+// pairs) at a time, the next chunk's loads in flight while the current one is
+// computed.
 constexpr int kZGroup = 1;
+static_assert(kZGroup == 1, "the staged-Z path reads one chunk at a time");
 
 __device__ __forceinline__ void load_z_group(const GemmParams& p, const uint16_t* zp, bool pairs, int row0, int col0,
                                              int c0, uint32_t (&zw)[4 * kZGroup]) {
@@ -246,17 +275,30 @@ __device__ __forceinline__ void load_z_group(const GemmParams& p, const uint16_t
     }
 }
 
-template <bool BGRAD>
+// Z words of chunk c (rows row0 + 8r) from the staged tile; zrow = the
+// thread's first row in its half's first box plus 4 * (lane % 4), g8 = row % 8.
+__device__ __forceinline__ void load_z_smem(const uint8_t* zrow, int g8, int c, uint32_t (&zw)[4]) {
+    const uint8_t* z = zrow + (c >> 3) * kZBoxBytes + (((c & 7) ^ g8) << 4);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) zw[r] = *reinterpret_cast<const uint32_t*>(z + r * 8 * 128);
+}
+
+template <bool BGRAD, bool ZSMEM>
 __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int col0,
-                                            const uint64_t (&acc)[4 * kChunks], float* band, int lane) {
+                                            const uint64_t (&acc)[4 * kChunks], float* band, int lane,
+                                            const uint8_t* zrow) {
     const bool pairs = (p.N & 1) == 0;
     uint16_t* out = static_cast<uint16_t*>(p.out);
     const uint16_t* zp = static_cast<const uint16_t*>(p.aux);
+    const int g8 = lane >> 2;
     uint32_t zcur[4 * kZGroup], znext[4 * kZGroup];
-    load_z_group(p, zp, pairs, row0, col0, 0, zcur);
+    if (!ZSMEM) load_z_group(p, zp, pairs, row0, col0, 0, zcur);
 #pragma unroll
     for (int c0 = 0; c0 < kChunks; c0 += kZGroup) {
-        if (c0 + kZGroup < kChunks) load_z_group(p, zp, pairs, row0, col0, c0 + kZGroup, znext);
+        if (ZSMEM)
+            load_z_smem(zrow, g8, c0, zcur);
+        else if (c0 + kZGroup < kChunks)
+            load_z_group(p, zp, pairs, row0, col0, c0 + kZGroup, znext);
 #pragma unroll
         for (int i = 0; i < kZGroup; ++i) {
             const int c = c0 + i;
@@ -299,7 +341,7 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
                 }
             }
         }
-        if (c0 + kZGroup < kChunks) {
+        if (!ZSMEM && c0 + kZGroup < kChunks) {
 #pragma unroll
             for (int j = 0; j < 4 * kZGroup; ++j) zcur[j] = znext[j];
         }
@@ -331,6 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&sm.acc_full[b]), 1);
             mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
         }
+        mbar_init(smem_addr(&sm.zfull), 1);
+        mbar_init(smem_addr(&sm.zempty), kEpiWarps);
         mbar_init(smem_addr(&sm.drain), 1);
         fence_mbar_init();
     }
@@ -342,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
+    uint8_t* const zs = reinterpret_cast<uint8_t*>(&sm) + sizeof(SmemLayout);  // Z tile (dgrad only)
+    const bool z_staged = uses_z<EPI>() && p.z_tma != 0;
 
     if (warp < kFirstEpiWarp) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
     if (warp == 0) {
@@ -420,6 +466,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    } else if (warp == 2) {
+        // ------------------------------------------- Z tile loader (dgrad)
+        if (z_staged && lane == 0) {
+            tma_prefetch_desc(&maps.z);
+            uint32_t zph = 0;
+            int nz = 0;
+            bool ok = true;
+            if (!p.debug_starve) {
+                for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+                    int g, mt, nt;
+                    decode_tile(p, t, g, mt, nt);
+                    // the previous tile's epilogue must have read the buffer
+                    if (!mbar_wait(smem_addr(&sm.zempty), zph ^ 1u, budget)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t zb = smem_addr(&sm.zfull);
+                    mbar_arrive_expect_tx(zb, kZBytes);
+#pragma unroll
+                    for (int j = 0; j < kBN / kZBoxCols; ++j)
+                        tma_load_2d(smem_addr(zs + j * kZBoxBytes), &maps.z, zb, nt * kBN + j * kZBoxCols,
+                                    mt * kBM);
+                    ++nz;
+                    zph ^= 1u;
+                }
+            }
+            if (!ok) record_status(p.status, kStatusTimeout);
+            // the last load must have landed before shared memory goes away
+            if (nz > 0) mbar_wait(smem_addr(&sm.zfull), static_cast<uint32_t>(nz - 1) & 1u, budget);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         int s = 0, ab = 0;
@@ -464,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g8 = lane >> 2;  // row within each 8-row group
         const int cq = lane & 3;   // column pair within each 8-column chunk
         int ab = 0, ss = 0;
-        uint32_t aph = 0, sph = 0;
+        uint32_t aph = 0, sph = 0, zph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
             int g, mt, nt;
@@ -476,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4 * kChunks; ++j) acc[j] = 0ull;
             const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(half * kHalfN);
-            if (EPI == kEpiDgelu || EPI == kEpiDgeluBgrad) {
+            if (uses_z<EPI>() && !z_staged) {
                 // the stored pre-activations of this tile are read once the K loop
                 // is done: ask for them in L2 now (each lane of a quad one of the
                 // quad's four rows; a row's 128 columns span at most three lines)
@@ -543,7 +619,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // bias-gradient partials of this warp's 32 rows -> workspace band (4*mt + q)
                 float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
                                                       : nullptr;
-                store_dgrad<EPI == kEpiDgeluBgrad>(p, row0, col0, acc, band, lane);
+                if (z_staged) {
+                    ok = warp_all(mbar_wait(smem_addr(&sm.zfull), zph, budget));
+                    if (!ok) break;
+                    const uint8_t* zrow = zs + half * (kHalfN / kZBoxCols) * kZBoxBytes + (q * 32 + g8) * 128 + 4 * cq;
+                    store_dgrad<EPI == kEpiDgeluBgrad, true>(p, row0, col0, acc, band, lane, zrow);
+                    // read with ordinary loads, refilled by TMA: order before the release
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&sm.zempty));
+                    zph ^= 1u;
+                } else {
+                    store_dgrad<EPI == kEpiDgeluBgrad, false>(p, row0, col0, acc, band, lane, nullptr);
+                }
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
@@ -566,11 +654,11 @@ int launch_gemm_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t s
         cudaFuncAttributes attr;
         if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess || attr.numRegs != kLaunchRegs) return -3;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
+                                 static_cast<int>(smem_bytes<EPI>())) != cudaSuccess)
             return -3;
         configured |= 1ull << dev;
     }
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
+    kern<<<grid, kThreads, smem_bytes<EPI>(), stream>>>(maps, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
                                                       : nullptr;
-                store_dgrad<EPI == kEpiDgeluBgrad>(p, row0, col0, acc, band, lane);
+                store_dgrad<EPI == kEpiDgeluBgrad, false>(p, row0, col0, acc, band, lane, nullptr);
             }
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);

@@ -36,6 +36,7 @@ struct GemmParams {
     int32_t total_tiles;
     int32_t accumulate;   // wgrad: 1 = out +=, 0 = out =
     int32_t debug_starve; // test hook: producer issues no loads
+    int32_t z_tma;        // dgrad: 1 = stored Z tiles staged in shared memory by TMA (maps.z)
     uint32_t idesc;       // tcgen05 instruction descriptor (formats, tile shape)
     uint64_t budget_ns;   // wall-clock budget of each pipeline wait
     void* out;            // bf16 [M][N] (fprop/dgrad) or fp32 [G][M][N] (wgrad)
@@ -52,6 +53,7 @@ struct GemmParams {
 
 struct TensorMaps {
     CUtensorMap a, b, sa, sb;
+    CUtensorMap z;  // dgrad with z_tma: Z bf16 [M][N] in 64 x 128 boxes, 128-byte swizzle
 };
 
 int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
@@ -70,6 +72,5 @@ int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, int fast, cud
 int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* bgrad, cudaStream_t stream,
                           int num_sms);
-size_t gemm_smem_bytes();
 
 }  // namespace fp8ll

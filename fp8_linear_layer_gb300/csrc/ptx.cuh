@@ -157,49 +157,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-// 32 lanes x 64 consecutive 32-bit columns: thread t of the warp receives the
-// 64 columns of TMEM lane (lane_base + t).  The load and its completion wait
-// are one asm statement, so the destination registers are defined only once
-// the data has arrived: the compiler cannot copy, spill or read them while the
-// asynchronous load is still writing them.
-__device__ __forceinline__ void tmem_ld_32x32b_x64_sync(uint32_t taddr, uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
-        : "memory");
-}
-
-// 32 lanes x 64 consecutive 32-bit columns, returned as 32 packed pairs
-// (column 2i in the low half of p[i]).  Load, completion wait and packing are
-// one asm statement: the destination registers are only defined once the data
-// has arrived, and the pairs come out of the load's consecutive registers.
-__device__ __forceinline__ void tmem_ld_32x32b_x64_pairs(uint32_t taddr, uint64_t (&p)[32]) {
-    asm volatile(
-        "{\n\t.reg .b32 t<64>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31, t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\tmov.b64 %16, {t32, t33};\n\tmov.b64 %17, {t34, t35};\n\tmov.b64 %18, {t36, t37};\n\tmov.b64 %19, {t38, t39};\n\tmov.b64 %20, {t40, t41};\n\tmov.b64 %21, {t42, t43};\n\tmov.b64 %22, {t44, t45};\n\tmov.b64 %23, {t46, t47};\n\tmov.b64 %24, {t48, t49};\n\tmov.b64 %25, {t50, t51};\n\tmov.b64 %26, {t52, t53};\n\tmov.b64 %27, {t54, t55};\n\tmov.b64 %28, {t56, t57};\n\tmov.b64 %29, {t58, t59};\n\tmov.b64 %30, {t60, t61};\n\tmov.b64 %31, {t62, t63};\n\t}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
-        : "r"(taddr)
-        : "memory");
-}
-
-// 32 consecutive columns of this warp's 32 TMEM lanes, returned as 16 packed
-// fp32 pairs; the wait is inside the same statement, so no use of the outputs
-// can be scheduled before the data has arrived.
-__device__ __forceinline__ void tmem_ld_32x32b_x32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
-    asm volatile(
-        "{\n\t.reg .b32 t<32>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {t0, t1};\n\tmov.b64 %1, {t2, t3};\n\tmov.b64 %2, {t4, t5};\n\tmov.b64 %3, {t6, t7};\n\tmov.b64 %4, {t8, t9};\n\tmov.b64 %5, {t10, t11};\n\tmov.b64 %6, {t12, t13};\n\tmov.b64 %7, {t14, t15};\n\tmov.b64 %8, {t16, t17};\n\tmov.b64 %9, {t18, t19};\n\tmov.b64 %10, {t20, t21};\n\tmov.b64 %11, {t22, t23};\n\tmov.b64 %12, {t24, t25};\n\tmov.b64 %13, {t26, t27};\n\tmov.b64 %14, {t28, t29};\n\tmov.b64 %15, {t30, t31};\n\t}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
-        : "r"(taddr)
-        : "memory");
-}
-
 // Two 16-lane TMEM loads of 32 columns each (shape 16x256b, 4 repetitions),
 // one at lane offset +0 and one at +16 of the warp's quadrant, completed by one
 // wait inside the same statement.  Fragment of thread t for repetition i
@@ -217,6 +174,7 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4_pairs2(uint32_t a, uint32_t b
         : "r"(a), "r"(b)
         : "memory");
 }
+
 // packed fp32x2 arithmetic on 64-bit register pairs (low half = first element);
 // each lane rounds to nearest exactly as the scalar mul / fma would
 __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
@@ -258,14 +216,6 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
     return d;
-}
-
-// Instruction descriptor for kind::f8f6f4, fp32 accumulator, both operands
-// K-major, M x N tile.  fmt: 0 = e4m3, 1 = e5m2.
-//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format,
-//   15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t make_idesc_f8(uint32_t fmt_a, uint32_t fmt_b, uint32_t M, uint32_t N) {
-    return (1u << 4) | (fmt_a << 7) | (fmt_b << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // ------------------------------------------------------------ conversions
