@@ -35,7 +35,7 @@ SEED = 1002  # base seed of the training-step workload
 WORKLOAD = "linear_train_step_m8192_k4096_n14336_bias_gelu"
 METRIC = "FP8 GEMM TFLOPS (fprop/dgrad/wgrad) and % of GB300 dense-FP8 peak, 1 GPU"
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor-core ratio on this part
-KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "common.cuh", "internal.h", "gemm_fprop.cu", "gemm_dgrad.cu",
+KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "common.cuh", "gemm_params.h", "gemm_fprop.cu", "gemm_dgrad.cu",
                   "gemm_wgrad.cu")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fp8_kernel_m8192_k4096_n14336_traffic.md")
 
@@ -563,6 +563,10 @@ def run_kernel_study(args):
     for fmt, nm in ((fp8.E4M3, "e4m3"), (fp8.E5M2, "e5m2")):
         out["cast_gbs"]["rows_%s_32768x8192" % nm] = gb / timed(lambda: fp8.quantize(xb, fmt))
         out["cast_gbs"]["transposed_%s_32768x8192" % nm] = gb / timed(lambda: fp8.quantize(xb, fmt, transpose=True))
+    # both orientations from one read: 2 bytes read, 2 x (1 + 4/128) written per element
+    gb2 = xb.numel() * (2.0 + 2.0 * (1.0 + 4.0 / 128)) / 1e6
+    qr, qt = fp8.empty_fp8(32768, 8192, fp8.E4M3), fp8.empty_fp8(8192, 32768, fp8.E4M3)
+    out["cast_gbs"]["dual_e4m3_32768x8192"] = gb2 / timed(lambda: fp8.quantize_dual(xb, fp8.E4M3, out=qr, out_t=qt))
     out["hbm_peak_gbs"] = peaks()[1]
     out["status"] = fp8.device_status()
     print(json.dumps(out))

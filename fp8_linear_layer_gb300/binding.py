@@ -9,7 +9,7 @@ device is not supported, calls raise.
 import ctypes
 import os
 from dataclasses import dataclass
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import torch
 
@@ -22,7 +22,7 @@ ACC_FULL, ACC_FAST = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 
 # every symbol include/fp8ll.h declares
-EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
+EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
            "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
            "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
            "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad")
@@ -60,6 +60,7 @@ def lib():
         L.fp8_scale_ld.argtypes = [i64]
         L.fp8_scale_ld.restype = i64
         L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, i64, vp]
+        L.fp8_quantize_dual.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, i64, vp]
         L.fp8_cast_f32.argtypes = [vp, i64, i32, vp, vp]
         L.fp8_gemm_fprop.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp]
         L.fp8_workspace_size.argtypes = [i64, i64]
@@ -79,7 +80,7 @@ def lib():
         L.fp8_mx_gemm_fprop.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp, vp, vp]
         L.fp8_mx_gemm_dgrad.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp, vp, vp, sz, vp]
         L.fp8_mx_gemm_wgrad.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp]
-        for name in ("fp8_quantize", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
+        for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
                      "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
                      "fp8_mx_gemm_wgrad",
                      "fp8_grouped_wgrad", "fp8_get_device_status", "fp8_debug_starve_next_gemm"):
@@ -145,6 +146,22 @@ def quantize(x: torch.Tensor, fmt: int, transpose: bool = False, out: Optional[F
     _check(lib().fp8_quantize(_ptr(x), rows, cols, x.stride(0), int(fmt), int(bool(transpose)), _ptr(out.q),
                               _ptr(out.scale), out.scale.stride(0), _stream()), "fp8_quantize")
     return out
+
+
+def quantize_dual(x: torch.Tensor, fmt: int, out: Optional[Fp8Tensor] = None,
+                  out_t: Optional[Fp8Tensor] = None) -> Tuple[Fp8Tensor, Fp8Tensor]:
+    """bf16 [rows][cols] -> (quantize(x, fmt), quantize(x, fmt, transpose=True))
+    from one read of x; rows and cols multiples of 128."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if out is None:
+        out = empty_fp8(rows, cols, fmt, x.device)
+    if out_t is None:
+        out_t = empty_fp8(cols, rows, fmt, x.device)
+    _check(lib().fp8_quantize_dual(_ptr(x), rows, cols, x.stride(0), int(fmt), _ptr(out.q), _ptr(out.scale),
+                                   out.scale.stride(0), _ptr(out_t.q), _ptr(out_t.scale), out_t.scale.stride(0),
+                                   _stream()), "fp8_quantize_dual")
+    return out, out_t
 
 
 def cast_f32(x: torch.Tensor, fmt: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:

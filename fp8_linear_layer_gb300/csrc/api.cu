@@ -261,6 +261,29 @@ int fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, in
                : FP8LL_ERR_LAUNCH;
 }
 
+int fp8_quantize_dual(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
+                      float* scale_rows, int64_t scale_ld_rows, uint8_t* q_cols, float* scale_cols,
+                      int64_t scale_ld_cols, fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !valid_fmt(fmt)) return FP8LL_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8LL_OK;
+    if (!x_bf16 || !q_rows || !scale_rows || !q_cols || !scale_cols) return FP8LL_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(q_rows) || !aligned16(scale_rows) || !aligned16(q_cols) ||
+        !aligned16(scale_cols))
+        return FP8LL_ERR_INVALID_ARG;
+    if (rows > (1LL << 31) - 1 || cols > (1LL << 31) - 1) return FP8LL_ERR_INVALID_ARG;
+    if (rows % 128 != 0 || cols % 128 != 0 || rows / 128 > 65535) return FP8LL_ERR_INVALID_ARG;
+    if (ldx < cols || ldx % 8 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (scale_ld_rows < rows || scale_ld_rows % 4 != 0 || scale_ld_cols < cols || scale_ld_cols % 4 != 0)
+        return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_quantize_dual(x_bf16, rows, cols, ldx, fmt, q_rows, scale_rows, scale_ld_rows, q_cols, scale_cols,
+                                scale_ld_cols, reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
 int fp8_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, fp8ll_stream_t stream) {
     if (n < 0 || !valid_fmt(fmt)) return FP8LL_ERR_INVALID_ARG;
     if (n == 0) return FP8LL_OK;

@@ -141,24 +141,52 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // The tile is staged in shared memory as 64 words per row (bf16 pairs), with
 // each 32-row band rotated by 8 words so that the column-wise reads of the
 // four 32-row parts hit 32 distinct banks.
-template <int FMT>
+//
+// With ROWS the CTA also writes the row-blocked cast of its tile (128 columns
+// = one block per row; codes qr [rows][cols], scales sr [cols/128][sldr]):
+// after the loads each half-warp holds one row's 128 values in registers, so
+// the row amax (a half-warp butterfly), scale and codes need no second read
+// of x.  The arithmetic is the row kernel's, so the codes are the same.
+template <int FMT, bool ROWS>
 __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
-                                                            float* __restrict__ scale, int64_t sld) {
+                                                            float* __restrict__ scale, int64_t sld,
+                                                            uint8_t* __restrict__ qr, float* __restrict__ sr,
+                                                            int64_t sldr) {
     __shared__ __align__(16) uint32_t tile[128][64];
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
 
+    // thread t, iteration it: row (t + 256 it) / 16 of the tile, columns
+    // 8 ((t + 256 it) % 16) .. +7; all eight loads are issued first
+    uint4 v[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int i = threadIdx.x + it * 256;
+        const int64_t c = c0 + (i & 15) * 8;
+        v[it] = make_uint4(0, 0, 0, 0);
+        if (c < cols) v[it] = __ldcs(reinterpret_cast<const uint4*>(x + (r0 + (i >> 4)) * ldx + c));
+    }
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int i = threadIdx.x + it * 256;
         const int rr = i >> 4;
         const int ch = i & 15;
-        const int64_t c = c0 + ch * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (c < cols) v = __ldcs(reinterpret_cast<const uint4*>(x + (r0 + rr) * ldx + c));
         const int w = (ch * 4 + 8 * (rr >> 5)) & 63;
-        *reinterpret_cast<uint4*>(&tile[rr][w]) = v;
+        *reinterpret_cast<uint4*>(&tile[rr][w]) = v[it];
+        if (ROWS) {
+            const float f[8] = {bf16_lo(v[it].x), bf16_hi(v[it].x), bf16_lo(v[it].y), bf16_hi(v[it].y),
+                                bf16_lo(v[it].z), bf16_hi(v[it].z), bf16_lo(v[it].w), bf16_hi(v[it].w)};
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+#pragma unroll
+            for (int off = 1; off <= 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            float inv, s;
+            block_scale<FMT>(amax, inv, s);
+            *reinterpret_cast<uint2*>(qr + (r0 + rr) * cols + c0 + ch * 8) = encode8<FMT>(f, inv);
+            if (ch == 0) sr[(c0 >> 7) * sldr + r0 + rr] = s;
+        }
     }
     __syncthreads();
 
@@ -416,10 +444,26 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
     } else {
         dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
         if (fmt == 0)
-            quantize_cols_kernel<0><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+            quantize_cols_kernel<0, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld, nullptr,
+                                                                      nullptr, 0);
         else
-            quantize_cols_kernel<1><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
+            quantize_cols_kernel<1, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld, nullptr,
+                                                                      nullptr, 0);
     }
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
+                         float* scale_rows, int64_t sld_rows, uint8_t* q_cols, float* scale_cols, int64_t sld_cols,
+                         cudaStream_t stream) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
+    if (fmt == 0)
+        quantize_cols_kernel<0, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols,
+                                                                 q_rows, scale_rows, sld_rows);
+    else
+        quantize_cols_kernel<1, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols,
+                                                                 q_rows, scale_rows, sld_rows);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -8,19 +8,23 @@ first), with e4m3 forward operands and e5m2 gradients ("FP8 GEMM for the fprop
 should use fast accumulation") and the accumulating fp32 weight gradient of
 "Weight gradient kernels for dense and MoE models":
 
-    X  (m x k) --quantize rows, e4m3-->  Xq          W (n x k) --rows, e4m3--> Wq
+    X  (m x k) --one read: rows, e4m3--> Xq,  columns, e4m3--> X^T (k x m)
+    W  (n x k) --rows, e4m3--> Wq
     fprop:  Z = Xq Wq^T + b,  Y = gelu(Z)          (bf16, Z kept)
     dY (m x k) --rows, e5m2--> dYq    (the gradient arriving through the next
                                        layer's weight, taken to be W^T)
     dgrad:  dZ = (dYq Wq^T) * gelu'(Z),  db = sum_tokens dZ      (bf16 dZ, fp32 db)
-    dZ^T --quantize down columns, e5m2-->  (n x m)     X^T --columns, e4m3--> (k x m)
+    dZ^T --quantize down columns, e5m2-->  (n x m)
     wgrad:  dW (n x k, fp32) += dZ^T X    (contraction over the m tokens)
     input gradient (optional, ``input_grad``):
             dZ --rows, e5m2--> dZq (m x n)    W --down columns, e4m3--> W^T (k x n)
             dX = dZq (W^T)^T = dZ W        (bf16, m x k, contraction over the n features)
 
-All buffers are allocated once (torch) so a step launches 9 kernels and
-allocates nothing; ``step`` can be captured in a CUDA graph.
+X is cast both ways by one kernel that reads it once (the transposed codes
+are kept for the weight gradient).  Built with ``input_grad=True``, the step
+also casts W and dZ both ways in one read each, and ``input_grad`` only runs
+its GEMM.  All buffers are allocated once (torch) so a step launches 8 kernels
+and allocates nothing; ``step`` can be captured in a CUDA graph.
 """
 import torch
 
@@ -28,10 +32,13 @@ from . import binding as B
 
 
 class LinearTrainStep:
-    def __init__(self, m: int, k: int, n: int, device="cuda", acc_mode: int = B.ACC_FULL):
+    def __init__(self, m: int, k: int, n: int, device="cuda", acc_mode: int = B.ACC_FULL,
+                 input_grad: bool = False):
         assert m % 128 == 0 and k % 128 == 0
+        assert not input_grad or n % 128 == 0, "the two-way casts of W and dZ need n % 128 == 0"
         self.m, self.k, self.n = m, k, n
         self.acc_mode = acc_mode
+        self.with_input_grad = input_grad
         dev = torch.device(device)
         self.Xq = B.empty_fp8(m, k, B.E4M3, dev)
         self.Wq = B.empty_fp8(n, k, B.E4M3, dev)
@@ -44,25 +51,57 @@ class LinearTrainStep:
         self.db = torch.empty((n,), dtype=torch.float32, device=dev)
         self.dW = torch.zeros((n, k), dtype=torch.float32, device=dev)
         self.ws = torch.empty((B.workspace_size(m, n) // 4,), dtype=torch.float32, device=dev)
+        if input_grad:
+            self._alloc_input_grad()
+
+    def _alloc_input_grad(self):
+        dev = self.dZ.device
+        self.dZq = B.empty_fp8(self.m, self.n, B.E5M2, dev)
+        self.WTq = B.empty_fp8(self.k, self.n, B.E4M3, dev)
+        self.dX = torch.empty((self.m, self.k), dtype=torch.bfloat16, device=dev)
 
     @property
     def gemm_flops(self) -> int:
         """Algorithmic flops of the three GEMMs of one step (2 m n k each)."""
         return 3 * 2 * self.m * self.n * self.k
 
+    # the step as a list of (kind, launch) pairs: forward, backward and the
+    # benchmark all run these
+    def _forward_plan(self, X, W, b):
+        if self.with_input_grad:
+            cast_w = ("quantize", lambda: B.quantize_dual(W, B.E4M3, out=self.Wq, out_t=self.WTq))
+        else:
+            cast_w = ("quantize", lambda: B.quantize(W, B.E4M3, out=self.Wq))
+        return [
+            ("quantize", lambda: B.quantize_dual(X, B.E4M3, out=self.Xq, out_t=self.XTq)),
+            cast_w,
+            ("gemm", lambda: B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y,
+                                          aux=self.Z)),
+        ]
+
+    def _backward_plan(self, X, dY):
+        if self.with_input_grad:
+            cast_dz = ("quantize", lambda: B.quantize_dual(self.dZ, B.E5M2, out=self.dZq, out_t=self.dZTq))
+        else:
+            cast_dz = ("quantize", lambda: B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq))
+        return [
+            ("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq)),
+            ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode,
+                                          out=self.dZ, bgrad=self.db, workspace=self.ws)),
+            cast_dz,
+            ("gemm", lambda: B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)),
+        ]
+
     def forward(self, X, W, b):
-        B.quantize(X, B.E4M3, out=self.Xq)
-        B.quantize(W, B.E4M3, out=self.Wq)
-        B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y, aux=self.Z)
+        for _, launch in self._forward_plan(X, W, b):
+            launch()
         return self.Y
 
     def backward(self, X, dY):
-        B.quantize(dY, B.E5M2, out=self.dYq)
-        B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode, out=self.dZ, bgrad=self.db,
-                     workspace=self.ws)
-        B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)
-        B.quantize(X, B.E4M3, transpose=True, out=self.XTq)
-        B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)
+        """dW += dZ^T X and db; X's transposed cast was made by ``forward``
+        (X is taken for the MXFP8 step, which casts it here)."""
+        for _, launch in self._backward_plan(X, dY):
+            launch()
         return self.dW, self.db
 
     def input_grad(self, W):
@@ -70,14 +109,13 @@ class LinearTrainStep:
         the backward GEMM of "How can we use te.Linear with weight parallel?"
         that contracts over the output features.  Both operands are cast with
         their 128-blocks along n (dZ by rows, W down its columns), so the GEMM is
-        the plain NT form without an epilogue.  Needs ``backward`` first."""
-        if not hasattr(self, "dX"):
-            dev = self.dZ.device
-            self.dZq = B.empty_fp8(self.m, self.n, B.E5M2, dev)
-            self.WTq = B.empty_fp8(self.k, self.n, B.E4M3, dev)
-            self.dX = torch.empty((self.m, self.k), dtype=torch.bfloat16, device=dev)
-        B.quantize(self.dZ, B.E5M2, out=self.dZq)
-        B.quantize(W, B.E4M3, transpose=True, out=self.WTq)
+        the plain NT form without an epilogue.  Needs ``backward`` first; with
+        ``input_grad=True`` the casts were already made by the step."""
+        if not self.with_input_grad:
+            if not hasattr(self, "dX"):
+                self._alloc_input_grad()
+            B.quantize(self.dZ, B.E5M2, out=self.dZq)
+            B.quantize(W, B.E4M3, transpose=True, out=self.WTq)
         B.gemm_fprop(self.dZq, self.WTq, None, B.EPI_NONE, self.acc_mode, out=self.dX)
         return self.dX
 
@@ -85,30 +123,18 @@ class LinearTrainStep:
         self.forward(X, W, b)
         return self.backward(X, dY)
 
-    # launch list of one step, for timing each kernel with events
     def launches(self, X, W, b, dY):
-        return [
-            ("quantize", lambda: B.quantize(X, B.E4M3, out=self.Xq)),
-            ("quantize", lambda: B.quantize(W, B.E4M3, out=self.Wq)),
-            ("gemm", lambda: B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y,
-                                          aux=self.Z)),
-            ("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq)),
-            ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode,
-                                          out=self.dZ, bgrad=self.db, workspace=self.ws)),
-            ("quantize", lambda: B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)),
-            ("quantize", lambda: B.quantize(X, B.E4M3, transpose=True, out=self.XTq)),
-            ("gemm", lambda: B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)),
-        ]
+        return self._forward_plan(X, W, b) + self._backward_plan(X, dY)
 
-    # 5 quantize + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
-    KERNELS_PER_STEP = 9
+    # 4 casts + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
+    KERNELS_PER_STEP = 8
 
 
 class MxLinearTrainStep(LinearTrainStep):
     """The same training step on MXFP8 operands: every cast puts one
     power-of-two scale on each 32 elements and every GEMM lets the tensor core
-    apply them (no software promotion).  Same buffers for the outputs, the
-    same 9 launches per step."""
+    apply them (no software promotion).  Same buffers for the outputs; 9
+    launches per step (X is cast once per orientation)."""
 
     def __init__(self, m: int, k: int, n: int, device="cuda"):
         assert m % 128 == 0 and k % 128 == 0
@@ -127,28 +153,15 @@ class MxLinearTrainStep(LinearTrainStep):
         self.dW = torch.zeros((n, k), dtype=torch.float32, device=dev)
         self.ws = torch.empty((B.workspace_size(m, n) // 4,), dtype=torch.float32, device=dev)
 
-    def forward(self, X, W, b):
-        B.mx_quantize(X, B.E4M3, out=self.Xq)
-        B.mx_quantize(W, B.E4M3, out=self.Wq)
-        B.mx_gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, out=self.Y, aux=self.Z)
-        return self.Y
-
-    def backward(self, X, dY):
-        B.mx_quantize(dY, B.E5M2, out=self.dYq)
-        B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ, bgrad=self.db, workspace=self.ws)
-        B.mx_quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)
-        B.mx_quantize(X, B.E4M3, transpose=True, out=self.XTq)
-        B.mx_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True)
-        return self.dW, self.db
-
-    def input_grad(self, W):
-        raise NotImplementedError("the input gradient is built for the 1x128 recipe")
-
-    def launches(self, X, W, b, dY):
+    def _forward_plan(self, X, W, b):
         return [
             ("quantize", lambda: B.mx_quantize(X, B.E4M3, out=self.Xq)),
             ("quantize", lambda: B.mx_quantize(W, B.E4M3, out=self.Wq)),
             ("gemm", lambda: B.mx_gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, out=self.Y, aux=self.Z)),
+        ]
+
+    def _backward_plan(self, X, dY):
+        return [
             ("quantize", lambda: B.mx_quantize(dY, B.E5M2, out=self.dYq)),
             ("gemm", lambda: B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ,
                                              bgrad=self.db, workspace=self.ws)),
@@ -157,3 +170,8 @@ class MxLinearTrainStep(LinearTrainStep):
             ("gemm", lambda: B.mx_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True)),
         ]
 
+    def input_grad(self, W):
+        raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+
+    # 5 casts + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
+    KERNELS_PER_STEP = 9

@@ -6,6 +6,7 @@
  * contraction dimension:
  *
  *   fp8_quantize        bf16 -> e4m3 / e5m2 codes + block scales
+ *   fp8_quantize_dual   both orientations of that cast from one read
  *   fp8_gemm_fprop      C = A B^T with bias / tanh-GELU epilogues, bf16 out
  *   fp8_gemm_dgrad      C = A B^T times gelu'(Z), optional bias-gradient sums
  *   fp8_gemm_wgrad      fp32 out (+)= A B^T
@@ -118,6 +119,27 @@ int64_t fp8_scale_ld(int64_t rows);
  * rows == 0 or cols == 0 is a no-op. */
 int fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose,
                  uint8_t* q, float* scale, int64_t scale_ld, fp8ll_stream_t stream);
+
+/* Both casts of fp8_quantize from one read of x: the row-blocked codes
+ * (transpose = 0) for the GEMMs that contract over the columns of x and the
+ * column-blocked, transposed codes (transpose = 1) for the weight-gradient
+ * GEMM that contracts over its rows.  "Weight gradient kernels for dense and
+ * MoE models" notes that separate cast launches around the GEMMs cost
+ * end-to-end time; here the activations that feed both GEMMs are read once
+ * instead of twice.  The outputs are bit-identical to the two separate
+ * fp8_quantize calls with the same fmt.
+ *   x:          bf16 [rows][ldx], 16-byte aligned, ldx % 8 == 0, ldx >= cols,
+ *               rows % 128 == 0, cols % 128 == 0, rows / 128 <= 65535.
+ *   q_rows:     [rows][cols];  scale_rows: [cols/128][scale_ld_rows],
+ *               scale_ld_rows >= rows.
+ *   q_cols:     [cols][rows];  scale_cols: [rows/128][scale_ld_cols],
+ *               scale_ld_cols >= cols.
+ * All outputs 16-byte aligned, scale leading dimensions % 4 == 0; the four
+ * output buffers must not overlap each other or x.  rows == 0 or cols == 0
+ * is a no-op. */
+int fp8_quantize_dual(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
+                      float* scale_rows, int64_t scale_ld_rows, uint8_t* q_cols, float* scale_cols,
+                      int64_t scale_ld_cols, fp8ll_stream_t stream);
 
 /* Element-wise fp32 -> fp8 code conversion with the same round-to-nearest-
  * even, saturating conversion the quantize kernel applies after scaling (no

@@ -65,6 +65,16 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.fp8_quantize(fake, 100, 128, 128, 0, 1, fake, fake, 128, None) == E  # rows % 128 != 0
     assert L.fp8_quantize(fake, 4, 128, 128, 0, 0, fake, fake, 3, None) == E      # scale_ld too small
     assert L.fp8_quantize(None, 0, 0, 0, 0, 0, None, None, 0, None) == 0          # empty is a no-op
+    # dual cast: both dimensions multiples of 128, both scale leading dimensions checked
+    assert L.fp8_quantize_dual(fake, 128, 200, 200, 0, fake, fake, 128, fake, fake, 200, None) == E  # cols % 128
+    assert L.fp8_quantize_dual(fake, 100, 256, 256, 0, fake, fake, 100, fake, fake, 256, None) == E  # rows % 128
+    assert L.fp8_quantize_dual(fake, 128, 256, 256, 2, fake, fake, 128, fake, fake, 256, None) == E  # format
+    assert L.fp8_quantize_dual(fake, 128, 256, 256, 0, fake, fake, 124, fake, fake, 256, None) == E  # row scales
+    assert L.fp8_quantize_dual(fake, 128, 256, 256, 0, fake, fake, 128, fake, fake, 252, None) == E  # col scales
+    assert L.fp8_quantize_dual(fake, 128, 256, 200, 0, fake, fake, 128, fake, fake, 256, None) == E  # ldx < cols
+    assert L.fp8_quantize_dual(fake, 128, 256, 256, 0, vp(0x10008), fake, 128, fake, fake, 256, None) == E
+    assert L.fp8_quantize_dual(fake, 128, 256, 256, 0, fake, fake, 128, None, fake, 256, None) == E
+    assert L.fp8_quantize_dual(None, 0, 256, 256, 0, None, None, 0, None, None, 0, None) == 0        # empty
     op = f.binding.OperandStruct(0x10000, 0x20000, 256, 8, 0, 0)
     bad = f.binding.OperandStruct(0x10000, 0x20000, 200, 8, 0, 0)   # ld_q % 16 != 0
     ob, oo = ctypes.byref(op), ctypes.byref(bad)

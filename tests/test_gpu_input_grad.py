@@ -52,3 +52,23 @@ def test_train_step_input_grad_matches_direct_call(fp8):
     ref, _ = fp8.gemm_fprop(A, Bt, None, fp8.EPI_NONE)
     torch.cuda.synchronize()
     assert torch.equal(dX, ref)
+
+
+def test_train_step_with_two_way_casts_is_bit_identical(fp8):
+    # input_grad=True casts X, W and dZ both ways in one read each; every
+    # output of the step and dX must equal the step built from single casts
+    from fp8_linear_layer_gb300.linear import LinearTrainStep
+    m, k, n = 384, 256, 640
+    X = workloads.normal_bf16((m, k), 73, "x").cuda()
+    W = workloads.normal_bf16((n, k), 73, "w", std=0.02).cuda()
+    b = workloads.normal_bf16((n,), 73, "b", std=0.02).cuda()
+    dY = workloads.normal_bf16((m, k), 73, "dy", std=1e-2).cuda()
+    plain, fused = LinearTrainStep(m, k, n), LinearTrainStep(m, k, n, input_grad=True)
+    outs = []
+    for st in (plain, fused):
+        st.step(X, W, b, dY)
+        outs.append((st.Y.clone(), st.Z.clone(), st.dZ.clone(), st.db.clone(), st.dW.clone(),
+                     st.input_grad(W).clone()))
+    torch.cuda.synchronize()
+    for a, c in zip(*outs):
+        assert torch.equal(a, c)

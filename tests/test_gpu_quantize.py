@@ -43,6 +43,52 @@ def test_transposed_exact(fp8, fmt, shape):
     check_exact(fp8, x, fmt, True)
 
 
+def check_dual(fp8, x, fmt):
+    """Both outputs of the one-read cast: exact against the oracle's row and
+    transposed casts, and bit-identical to the two separate kernels."""
+    xd = x.cuda()
+    tr, tc = fp8.quantize_dual(xd, fmt)
+    sr, sc = fp8.quantize(xd, fmt), fp8.quantize(xd, fmt, transpose=True)
+    torch.cuda.synchronize()
+    rows, cols = x.shape
+    for t, s, transpose, n in ((tr, sr, False, rows), (tc, sc, True, cols)):
+        q, sb = t.q.cpu().numpy(), t.scale.cpu().numpy()[:, :n]
+        qo, so = oracle.quantize(workloads.bits(x), fmt, transpose=transpose)
+        assert np.array_equal(q, qo), "codes differ at %s" % (np.argwhere(q != qo)[:5].tolist(),)
+        assert np.array_equal(sb.view(np.uint32), so.view(np.uint32)), "scale bits differ"
+        assert torch.equal(t.q, s.q)
+        assert np.array_equal(sb.view(np.uint32), s.scale.cpu().numpy()[:, :n].view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (640, 256), (1024, 1152)])
+def test_dual_exact(fp8, fmt, shape):
+    x = workloads.normal_bf16(shape, 400 + fmt, "dq", std=1.5)
+    check_dual(fp8, x, fmt)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_dual_strided_and_special(fp8, fmt):
+    # a row stride wider than the matrix, plus the special blocks of the test below
+    x = workloads.normal_bf16((256, 640), 9, "dsp", std=1.0).float()
+    x[0, :] = 0.0
+    x[1, :128] = -0.0
+    x[2, :128] = 1e-38
+    x[3, 128:256] = 3e38
+    x[:, 9] *= 64.0
+    x[:128, 300] = 0.0
+    wide = torch.zeros((256, 768), dtype=torch.bfloat16)
+    wide[:, :640] = x.to(torch.bfloat16)
+    xv = wide.cuda()[:, :640]
+    tr, tc = fp8.quantize_dual(xv, fmt)
+    torch.cuda.synchronize()
+    xb = x.to(torch.bfloat16)
+    for t, transpose, n in ((tr, False, 256), (tc, True, 640)):
+        qo, so = oracle.quantize(workloads.bits(xb), fmt, transpose=transpose)
+        assert np.array_equal(t.q.cpu().numpy(), qo)
+        assert np.array_equal(t.scale.cpu().numpy()[:, :n].view(np.uint32), so.view(np.uint32))
+
+
 @pytest.mark.parametrize("fmt", [0, 1])
 @pytest.mark.parametrize("transpose", [False, True])
 def test_special_blocks(fp8, fmt, transpose):
