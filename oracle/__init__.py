@@ -15,7 +15,8 @@ Sources, by page title:
     weight-gradient GEMM that ACCUMULATES (out += a b^T), its k-grouped MoE
     variant, the per-token 1x128 cast of both operands.
   * "FP8 GEMM for the fprop should use fast accumulation": e4m3 forward,
-    e4m3 x e5m2 backward, fast vs full accumulation as an explicit flag.
+    e4m3 x e5m2 backward, fast vs full accumulation as an explicit flag,
+    per-tensor scales (with which fast accumulation needs no promotion).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (closed forms, brute force over exact rationals, the worked example on the
@@ -60,6 +61,10 @@ def _load():
                                     vp, i64, vp, i64, vp, vp]
         lib.oracle_mx_quantize.argtypes = [i32, vp, i64, i64, i64, i32, vp, vp, i64]
         lib.oracle_mx_gemm.argtypes = [i64, vp, i64, vp, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp, i64, vp, vp]
+        f32 = ctypes.c_float
+        lib.oracle_tensor_quantize.argtypes = [i32, vp, i64, i64, i64, i32, f32, vp, vp, vp]
+        lib.oracle_amax_history.argtypes = [vp, i64, f32, vp]
+        lib.oracle_tensor_gemm.argtypes = [i64, i64, i64, vp, i64, f32, i32, vp, i64, f32, i32, vp, vp]
         lib.oracle_gelu.argtypes = [ctypes.c_double]
         lib.oracle_gelu.restype = ctypes.c_double
         lib.oracle_dgelu.argtypes = [ctypes.c_double]
@@ -226,6 +231,47 @@ def mx_gemm(qa, ea, fmt_a, qb, eb, fmt_b, rows=None, cols=None, want_abs=True):
     _load().oracle_mx_gemm(K, _p(qa), K, _p(ea), ea.shape[1], int(fmt_a), _p(qb), K, _p(eb), eb.shape[1],
                            int(fmt_b), None if r is None else _p(r), nr, None if c is None else _p(c), nc,
                            _p(acc), None if S is None else _p(S))
+    return acc, S
+
+
+# ------------------------------------------------------ per-tensor scaling ----
+
+def tensor_quantize(x_bits, fmt: int, amax_in: float, transpose: bool = False):
+    """Per-tensor cast of a bf16 matrix (bit patterns, [rows][cols]) with one
+    scale from the given amax: inv = fl32(FMAX/amax), scale = fl32(amax/FMAX),
+    q = enc(fl32(x inv)), saturating above amax.  Returns (q, scale, amax of
+    x); q is [rows][cols], or [cols][rows] with transpose=True."""
+    x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
+    rows, cols = x.shape
+    q = np.empty((cols, rows) if transpose else (rows, cols), dtype=np.uint8)
+    sc = np.empty(1, dtype=np.float32)
+    am = np.empty(1, dtype=np.float32)
+    _load().oracle_tensor_quantize(int(fmt), _p(x), rows, cols, cols, int(bool(transpose)),
+                                   float(np.float32(amax_in)), _p(q), _p(sc), _p(am))
+    return q, sc[0], am[0]
+
+
+def amax_history(hist, amax_new: float):
+    """Delayed scaling: push amax_new to the front of the history (the oldest
+    entry drops out); returns (updated history, largest entry)."""
+    h = np.array(hist, dtype=np.float32, copy=True)
+    use = np.empty(1, dtype=np.float32)
+    _load().oracle_amax_history(_p(h), h.size, float(np.float32(amax_new)), _p(use))
+    return h, use[0]
+
+
+def tensor_gemm(qa, sa: float, fmt_a, qb, sb: float, fmt_b, want_abs=True):
+    """Per-tensor scaled "nt" GEMM in float64: acc[i][j] = sa sb sum_k
+    dec(qa[i,k]) dec(qb[j,k]); returns (acc, S), S the same sum of |products|."""
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qb = np.ascontiguousarray(qb, dtype=np.uint8)
+    M, K = qa.shape
+    N, K2 = qb.shape
+    assert K == K2
+    acc = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64) if want_abs else None
+    _load().oracle_tensor_gemm(M, N, K, _p(qa), K, float(np.float32(sa)), int(fmt_a), _p(qb), K,
+                               float(np.float32(sb)), int(fmt_b), _p(acc), None if S is None else _p(S))
     return acc, S
 
 

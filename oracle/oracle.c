@@ -18,7 +18,8 @@
  *       MoE variant, the per-token (1x128) cast of both operands, and the
  *       worked ones/rand example.
  *  [P4] "FP8 GEMM for the fprop should use fast accumulation" -- e4m3 for the
- *       forward GEMM, e5m2 on the gradient side, fast vs full accumulation.
+ *       forward GEMM, e5m2 on the gradient side, fast vs full accumulation,
+ *       per-tensor scales.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - fp8 bit layouts are the OCP FP8 definitions (the pages only name e4m3 and
@@ -368,6 +369,88 @@ void oracle_mx_gemm(int64_t K,
             }
             acc[ii * ncols + jj] = total;
             if (S) S[ii * ncols + jj] = total_abs;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* per-tensor scaling ([P4]: one scale per operand tensor, taken from an amax  */
+/* history -- "delayed scaling" -- or from the tensor itself; with it the      */
+/* fast-accumulation GEMM needs no promotion inside the K loop)              */
+/* ------------------------------------------------------------------------ */
+
+/* One scale for the whole tensor from a given amax A (the tensor's own amax, or
+ * the largest amax of earlier steps): inv = fl32(FMAX/A), scale = fl32(A/FMAX),
+ * q = enc(fl32(x*inv)) -- the same reading as the per-block cast, with the
+ * block widened to the tensor.  A = 0, or FMAX/A overflowing binary32, gives
+ * inv = scale = 1.  Values above A saturate to +-FMAX (a delayed amax may be
+ * smaller than the tensor's own).  amax_out = max|x| of this tensor, exact.
+ * transpose == 0: q [rows][cols]; transpose == 1: q [cols][rows]. */
+void oracle_tensor_quantize(int fmt, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                            int transpose, float amax_in, uint8_t* q, float* scale_out, float* amax_out)
+{
+    build_tables();
+    const float fmax = (float)oracle_fp8_max(fmt);
+    float inv = 1.0f, scale = 1.0f;
+    if (amax_in > 0.0f) {
+        const float t = fmax / amax_in; /* binary32 division */
+        if (t <= FLT_MAX) {
+            inv = t;
+            scale = amax_in / fmax; /* binary32 division */
+        }
+    }
+    *scale_out = scale;
+    float amax = 0.0f;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            const float v = oracle_bf16_to_f32(x[r * ldx + c]);
+            const float a = fabsf(v);
+            if (a > amax) amax = a;
+            const uint8_t code = oracle_fp8_encode(fmt, v * inv); /* binary32 product */
+            if (transpose)
+                q[c * rows + r] = code;
+            else
+                q[r * cols + c] = code;
+        }
+    }
+    *amax_out = amax;
+}
+
+/* Amax history of delayed scaling: the new amax enters at position 0, every
+ * older entry moves one place back (the oldest drops out), and the amax to
+ * scale the next cast with is the largest entry of the updated history. */
+void oracle_amax_history(float* hist, int64_t len, float amax_new, float* amax_use)
+{
+    for (int64_t i = len - 1; i > 0; --i) hist[i] = hist[i - 1];
+    hist[0] = amax_new;
+    float m = 0.0f;
+    for (int64_t i = 0; i < len; ++i)
+        if (hist[i] > m) m = hist[i];
+    *amax_use = m;
+}
+
+/* acc[i][j] = sa * sb * sum_k dec(qa[i][k]) dec(qb[j][k]) and S the same sum of
+ * absolute values, binary64, for all rows x cols; both operands K-major. */
+void oracle_tensor_gemm(int64_t M, int64_t N, int64_t K,
+                        const uint8_t* qa, int64_t lda, float sa, int fmt_a,
+                        const uint8_t* qb, int64_t ldb, float sb, int fmt_b,
+                        double* acc, double* S)
+{
+    build_tables();
+    const double* ta = g_table[fmt_a ? 1 : 0];
+    const double* tb = g_table[fmt_b ? 1 : 0];
+    const double s = (double)sa * (double)sb;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double total = 0.0, total_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = ta[qa[i * lda + k]] * tb[qb[j * ldb + k]];
+                total += p;
+                total_abs += fabs(p);
+            }
+            acc[i * N + j] = s * total;
+            if (S) S[i * N + j] = fabs(s) * total_abs;
         }
     }
 }

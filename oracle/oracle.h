@@ -58,6 +58,15 @@ void oracle_mx_gemm(int64_t K,
                     const int64_t* rows, int64_t nrows, const int64_t* cols, int64_t ncols,
                     double* acc, double* S);
 
+/* per-tensor scaling: cast from a given amax, amax history, GEMM */
+void oracle_tensor_quantize(int fmt, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                            int transpose, float amax_in, uint8_t* q, float* scale_out, float* amax_out);
+void oracle_amax_history(float* hist, int64_t len, float amax_new, float* amax_use);
+void oracle_tensor_gemm(int64_t M, int64_t N, int64_t K,
+                        const uint8_t* qa, int64_t lda, float sa, int fmt_a,
+                        const uint8_t* qb, int64_t ldb, float sb, int fmt_b,
+                        double* acc, double* S);
+
 double oracle_gelu(double z);
 double oracle_dgelu(double z);
 void   oracle_gelu_array(const double* z, double* y, int64_t n);
