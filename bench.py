@@ -74,9 +74,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--acc", choices=["full", "fast"], default="full")
-    ap.add_argument("--recipe", choices=["block128", "mx"], default="block128",
+    ap.add_argument("--recipe", choices=["block128", "mx", "tensor"], default="block128",
                     help="block128: one fp32 scale per 128 elements, promoted in software (the configured "
-                         "workload); mx: MXFP8, one power-of-two scale per 32 elements applied by the tensor core")
+                         "workload); mx: MXFP8, one power-of-two scale per 32 elements applied by the tensor core; "
+                         "tensor: one scale per tensor (delayed scaling), scaled once after the K loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
@@ -349,6 +350,9 @@ def run_ours(args):
     if args.recipe == "mx":
         from fp8_linear_layer_gb300.linear import MxLinearTrainStep
         step = MxLinearTrainStep(m, k, n, dev)
+    elif args.recipe == "tensor":
+        from fp8_linear_layer_gb300.linear import TensorLinearTrainStep
+        step = TensorLinearTrainStep(m, k, n, dev)
     else:
         step = LinearTrainStep(m, k, n, dev, acc_mode)
     launches = step.launches(X, W, b, dY)
@@ -419,13 +423,14 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8(e4m3/e5m2) x fp8 -> fp32 accumulate", "data": "synthetic",
             "config": {"workload": (WORKLOAD if default_size else "linear_train_step_m%d_k%d_n%d_bias_gelu" % (m, k, n))
-                       + ("_mxfp8" if args.recipe == "mx" else ""),
+                       + {"block128": "", "mx": "_mxfp8", "tensor": "_per_tensor_delayed"}[args.recipe],
                        "m_tokens": m, "k_in": k, "n_out": n,
                        "acc_mode": args.acc if args.recipe == "block128" else None, "recipe": args.recipe,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
-            "roofline": {"bound": "tensor", "kernel": ("gemm_mx_kernel" if args.recipe == "mx" else "gemm_fp8_kernel")
+            "roofline": {"bound": "tensor", "kernel": {"block128": "gemm_fp8_kernel", "mx": "gemm_mx_kernel",
+                                                       "tensor": "gemm_mx_kernel<TENSOR>"}[args.recipe]
                          + " (fprop, dgrad, wgrad launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),

@@ -25,7 +25,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSP
 EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
            "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
            "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
-           "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad")
+           "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize",
+           "fp8_amax_history_update", "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad")
 
 
 class Fp8Error(RuntimeError):
@@ -42,6 +43,11 @@ class OperandStruct(ctypes.Structure):
 class MxOperandStruct(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("ld_q", ctypes.c_int64), ("fmt", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class TensorOperandStruct(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("ld_q", ctypes.c_int64),
+                ("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -80,9 +86,17 @@ def lib():
         L.fp8_mx_gemm_fprop.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp, vp, vp]
         L.fp8_mx_gemm_dgrad.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp, vp, vp, sz, vp]
         L.fp8_mx_gemm_wgrad.argtypes = [i64, i64, i64, mop, mop, vp, i32, vp]
+        top = ctypes.POINTER(TensorOperandStruct)
+        L.fp8_tensor_amax.argtypes = [vp, i64, i64, i64, vp, vp]
+        L.fp8_tensor_quantize.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
+        L.fp8_amax_history_update.argtypes = [vp, i64, vp, vp, vp]
+        L.fp8_tensor_gemm_fprop.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp]
+        L.fp8_tensor_gemm_dgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp, sz, vp]
+        L.fp8_tensor_gemm_wgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp]
         for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
                      "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
-                     "fp8_mx_gemm_wgrad",
+                     "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize", "fp8_amax_history_update",
+                     "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
                      "fp8_grouped_wgrad", "fp8_get_device_status", "fp8_debug_starve_next_gemm"):
             getattr(L, name).restype = i32
         _lib = L
@@ -338,4 +352,121 @@ def mx_gemm_wgrad(A: Fp8MxTensor, B: Fp8MxTensor, out: torch.Tensor, accumulate:
     oa, ob = A.operand(), B.operand()
     _check(lib().fp8_mx_gemm_wgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(out), int(bool(accumulate)),
                                    _stream()), "fp8_mx_gemm_wgrad")
+    return out
+
+
+# ------------------------------------------------------ per-tensor scaling ----
+
+@dataclass
+class Fp8TensorScaled:
+    """fp8 codes [rows][ld_q] (uint8) with the tensor's one fp32 scale (a
+    1-element device tensor)."""
+    q: torch.Tensor
+    scale: torch.Tensor
+    fmt: int
+
+    @property
+    def rows(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.q.shape[1]
+
+    def operand(self) -> TensorOperandStruct:
+        return TensorOperandStruct(self.q.data_ptr(), self.scale.data_ptr(), self.q.stride(0), int(self.fmt), 0)
+
+
+def empty_tensor_scaled(rows: int, k: int, fmt: int, device="cuda") -> Fp8TensorScaled:
+    return Fp8TensorScaled(torch.empty((rows, k), dtype=torch.uint8, device=device),
+                           torch.empty((1,), dtype=torch.float32, device=device), fmt)
+
+
+def tensor_amax(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """max|x| of a bf16 matrix into a 1-element fp32 device tensor."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    if out is None:
+        out = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _check(lib().fp8_tensor_amax(_ptr(x), x.shape[0], x.shape[1], x.stride(0), _ptr(out), _stream()),
+           "fp8_tensor_amax")
+    return out
+
+
+def tensor_quantize(x: torch.Tensor, fmt: int, amax_in: torch.Tensor, rows: bool = True, cols: bool = False,
+                    amax_out: Optional[torch.Tensor] = None, out: Optional[Fp8TensorScaled] = None,
+                    out_t: Optional[Fp8TensorScaled] = None):
+    """Per-tensor cast of bf16 x [r][c] with the amax in amax_in (1-element
+    device tensor).  rows: codes [r][c]; cols: transposed codes [c][r]; both
+    share the one scale.  Returns (rows operand or None, cols operand or None)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1 and (rows or cols)
+    r, c = x.shape
+    scale = out.scale if out is not None else (out_t.scale if out_t is not None else None)
+    if scale is None:
+        scale = torch.empty((1,), dtype=torch.float32, device=x.device)
+    if rows and out is None:
+        out = Fp8TensorScaled(torch.empty((r, c), dtype=torch.uint8, device=x.device), scale, fmt)
+    if cols and out_t is None:
+        out_t = Fp8TensorScaled(torch.empty((c, r), dtype=torch.uint8, device=x.device), scale, fmt)
+    if rows and cols:
+        assert out.scale.data_ptr() == out_t.scale.data_ptr(), "both orientations share one scale"
+    _check(lib().fp8_tensor_quantize(_ptr(x), r, c, x.stride(0), int(fmt), _ptr(amax_in),
+                                     _ptr(out.q) if rows else None, _ptr(out_t.q) if cols else None, _ptr(scale),
+                                     _ptr(amax_out), _stream()), "fp8_tensor_quantize")
+    return (out if rows else None), (out_t if cols else None)
+
+
+def amax_history_update(history: torch.Tensor, amax_new: torch.Tensor, amax_use: torch.Tensor) -> torch.Tensor:
+    """Delayed scaling: push amax_new into history (fp32 device tensors) and
+    write the largest entry to amax_use."""
+    assert history.dtype == torch.float32 and history.is_contiguous()
+    _check(lib().fp8_amax_history_update(_ptr(history), history.numel(), _ptr(amax_new), _ptr(amax_use), _stream()),
+           "fp8_amax_history_update")
+    return amax_use
+
+
+def tensor_gemm_fprop(A: Fp8TensorScaled, B: Fp8TensorScaled, bias: Optional[torch.Tensor] = None,
+                      epi: int = EPI_BIAS_GELU, out: Optional[torch.Tensor] = None,
+                      aux: Optional[torch.Tensor] = None, want_aux: bool = True):
+    """Y (bf16 [M][N]) = epilogue(sA sB A B^T); returns (Y, Z-or-None)."""
+    M, N, K = A.rows, B.rows, A.k
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if aux is None and want_aux and epi == EPI_BIAS_GELU:
+        aux = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_tensor_gemm_fprop(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(bias), int(epi),
+                                       _ptr(out), _ptr(aux), _stream()), "fp8_tensor_gemm_fprop")
+    return out, aux
+
+
+def tensor_gemm_dgrad(A: Fp8TensorScaled, B: Fp8TensorScaled, aux: torch.Tensor, epi: int = EPI_DGELU_BGRAD,
+                      out: Optional[torch.Tensor] = None, bgrad: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None):
+    """dZ (bf16 [M][N]) = (sA sB A B^T) * gelu'(aux) (+ bias gradient [N])."""
+    M, N, K = A.rows, B.rows, A.k
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = 0
+    if epi == EPI_DGELU_BGRAD:
+        if bgrad is None:
+            bgrad = torch.empty((N,), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty((workspace_size(M, N) // 4,), dtype=torch.float32, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_tensor_gemm_dgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(aux), int(epi), _ptr(out),
+                                       _ptr(bgrad), _ptr(workspace), ws_bytes, _stream()), "fp8_tensor_gemm_dgrad")
+    return out, bgrad
+
+
+def tensor_gemm_wgrad(A: Fp8TensorScaled, B: Fp8TensorScaled, out: torch.Tensor,
+                      accumulate: bool = True) -> torch.Tensor:
+    """fp32 out [M][N] (+)= sA sB A B^T."""
+    M, N, K = A.rows, B.rows, A.k
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (M, N)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_tensor_gemm_wgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                       int(bool(accumulate)), _stream()), "fp8_tensor_gemm_wgrad")
     return out

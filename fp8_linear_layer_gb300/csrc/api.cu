@@ -229,6 +229,34 @@ int mx_setup(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const
     return FP8LL_OK;
 }
 
+bool valid_tensor_operand(const fp8ll_tensor_operand_t* op, int64_t rows, int64_t K) {
+    if (!op || !op->q || !op->scale || !valid_fmt(op->fmt)) return false;
+    if (!aligned16(op->q) || (reinterpret_cast<uintptr_t>(op->scale) & 3u) != 0) return false;
+    if (op->ld_q < K || op->ld_q % 16 != 0 || op->ld_q >= (1LL << 39)) return false;
+    if (rows < 1 || rows > (1LL << 31) - 1) return false;
+    return true;
+}
+
+// shared setup of the three per-tensor GEMM entry points
+int tensor_setup(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A, const fp8ll_tensor_operand_t* B,
+                 TensorMaps& maps, GemmParams& p, DeviceInfo** dev) {
+    if (!valid_mn(M, N) || K < 128 || K % 128 != 0 || K >= (1LL << 36)) return FP8LL_ERR_INVALID_ARG;
+    if (!valid_tensor_operand(A, M, K) || !valid_tensor_operand(B, N, K)) return FP8LL_ERR_INVALID_ARG;
+    int rc = current_device(dev);
+    if (rc != FP8LL_OK) return rc;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_codes(A->q, A->ld_q, M, K, 128, &maps.a) || !encode_codes(B->q, B->ld_q, N, K, kTileN, &maps.b))
+        return FP8LL_ERR_LAUNCH;
+    fp8ll_operand_t pa{A->q, A->scale, A->ld_q, 0, A->fmt, 0}, pb{B->q, B->scale, B->ld_q, 0, B->fmt, 0};
+    init_params(p, M, N, &pa, &pb, *dev);  // the plain kind::f8f6f4 instruction descriptor
+    p.num_groups = 1;
+    p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
+    p.total_tiles = p.tiles_per_group;
+    p.tsa = A->scale;
+    p.tsb = B->scale;
+    return FP8LL_OK;
+}
+
 }  // namespace
 }  // namespace fp8ll
 
@@ -566,6 +594,119 @@ int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
     p.out = out;
     p.accumulate = accumulate;
     return launch_gemm_mx(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+
+int fp8_tensor_amax(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, float* amax,
+                    fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !amax || (reinterpret_cast<uintptr_t>(amax) & 3u) != 0) return FP8LL_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0) {
+        if (!x_bf16 || !aligned16(x_bf16) || cols % 8 != 0 || ldx < cols || ldx % 8 != 0)
+            return FP8LL_ERR_INVALID_ARG;
+    }
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0 || cols == 0) return cudaMemsetAsync(amax, 0, sizeof(float), s) == cudaSuccess ? FP8LL_OK
+                                                                                                  : FP8LL_ERR_LAUNCH;
+    return launch_tensor_amax(x_bf16, rows, cols, ldx, amax, s, dev->num_sms) == 0 ? FP8LL_OK : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_tensor_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
+                        uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !valid_fmt(fmt)) return FP8LL_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8LL_OK;
+    if (!x_bf16 || !aligned16(x_bf16) || !amax_in || !scale || (!q_rows && !q_cols)) return FP8LL_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(amax_in) & 3u) != 0 || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0)
+        return FP8LL_ERR_INVALID_ARG;
+    if (amax_out && ((reinterpret_cast<uintptr_t>(amax_out) & 3u) != 0 || amax_out == amax_in))
+        return FP8LL_ERR_INVALID_ARG;
+    if (rows > (1LL << 31) - 1 || cols > (1LL << 31) - 1 || ldx < cols || ldx % 8 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (q_rows && (!aligned16(q_rows) || cols % 16 != 0)) return FP8LL_ERR_INVALID_ARG;
+    if (q_cols && (!aligned16(q_cols) || rows % 128 != 0 || cols % 8 != 0 || rows / 128 > 65535))
+        return FP8LL_ERR_INVALID_ARG;
+    if (q_rows && q_cols && cols % 128 != 0) return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_tensor_quantize(x_bf16, rows, cols, ldx, fmt, amax_in, q_rows, q_cols, scale, amax_out,
+                                  reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_amax_history_update(float* history, int64_t len, const float* amax_new, float* amax_use,
+                            fp8ll_stream_t stream) {
+    if (!history || len < 1 || len > (1 << 20) || !amax_new || !amax_use) return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_amax_history(history, len, amax_new, amax_use, reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_tensor_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A,
+                          const fp8ll_tensor_operand_t* B, const void* bias_bf16, int epi, void* out_bf16,
+                          void* aux_bf16, fp8ll_stream_t stream) {
+    if (epi != FP8LL_EPI_NONE && epi != FP8LL_EPI_BIAS && epi != FP8LL_EPI_BIAS_GELU) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi != FP8LL_EPI_NONE && (!bias_bf16 || !aligned16(bias_bf16))) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    TensorMaps maps;
+    GemmParams p;
+    DeviceInfo* dev = nullptr;
+    int rc = tensor_setup(M, N, K, A, B, maps, p, &dev);
+    if (rc != FP8LL_OK) return rc;
+    p.out = out_bf16;
+    p.aux = (epi == FP8LL_EPI_BIAS_GELU) ? aux_bf16 : nullptr;
+    p.bias = bias_bf16;
+    return launch_gemm_tensor(maps, p, epi, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
+int fp8_tensor_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A,
+                          const fp8ll_tensor_operand_t* B, const void* aux_bf16, int epi, void* out_bf16, float* bgrad,
+                          void* workspace, size_t workspace_bytes, fp8ll_stream_t stream) {
+    if (epi != FP8LL_EPI_DGELU && epi != FP8LL_EPI_DGELU_BGRAD) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16) || !aux_bf16 || !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_DGELU_BGRAD) {
+        if (!bgrad || !aligned16(bgrad)) return FP8LL_ERR_INVALID_ARG;
+        if (!workspace || !aligned16(workspace) || workspace_bytes < fp8_workspace_size(M, N))
+            return FP8LL_ERR_WORKSPACE;
+    }
+    TensorMaps maps;
+    GemmParams p;
+    DeviceInfo* dev = nullptr;
+    int rc = tensor_setup(M, N, K, A, B, maps, p, &dev);
+    if (rc != FP8LL_OK) return rc;
+    p.out = out_bf16;
+    p.aux = const_cast<void*>(aux_bf16);
+    p.workspace = static_cast<float*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_gemm_tensor(maps, p, epi, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
+    if (epi == FP8LL_EPI_DGELU_BGRAD &&
+        launch_bgrad_finalize(static_cast<const float*>(workspace), static_cast<int64_t>(p.num_m_tiles) * 4, N, bgrad,
+                              s, dev->num_sms) != 0)
+        return FP8LL_ERR_LAUNCH;
+    return FP8LL_OK;
+}
+
+int fp8_tensor_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A,
+                          const fp8ll_tensor_operand_t* B, float* out, int accumulate, fp8ll_stream_t stream) {
+    if (!out || !aligned16(out) || (accumulate != 0 && accumulate != 1)) return FP8LL_ERR_INVALID_ARG;
+    TensorMaps maps;
+    GemmParams p;
+    DeviceInfo* dev = nullptr;
+    int rc = tensor_setup(M, N, K, A, B, maps, p, &dev);
+    if (rc != FP8LL_OK) return rc;
+    p.out = out;
+    p.accumulate = accumulate;
+    return launch_gemm_tensor(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }

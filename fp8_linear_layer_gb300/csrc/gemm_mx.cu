@@ -19,6 +19,12 @@
 //               fragments, as in the 1x128 kernel), handed back to the MMA
 //               warp, and stored through the same epilogue functions.
 // The scale atoms are the layout the MX cast writes (see quantize.cu).
+//
+// TENSOR = true is the per-tensor scaled GEMM ("FP8 GEMM for the fprop should
+// use fast accumulation": one scale per operand tensor): no scale atoms, plain
+// kind::f8f6f4 MMAs accumulate the raw fp8 products over the whole K range in
+// the same TMEM accumulator, and the epilogue multiplies the fp32 sums by
+// fl32(sA * sB) once -- no promotion inside the K loop.
 #include "gemm_kernel.cuh"
 
 namespace fp8ll {
@@ -72,7 +78,7 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t adesc, uint64_t bdes
         : "memory");
 }
 
-template <int EPI>
+template <int EPI, bool TENSOR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -123,13 +129,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         const uint32_t fb = smem_addr(&sm.full[s]);
-                        mbar_arrive_expect_tx(fb, kBM * kBK + kBN * kBK + 512 + 1024);
+                        mbar_arrive_expect_tx(fb, kBM * kBK + kBN * kBK + (TENSOR ? 0 : 512 + 1024));
                         tma_load_2d(smem_addr(sm.a[s]), &maps.a, fb, kb * kBK, m0);
                         tma_load_2d(smem_addr(sm.b[s]), &maps.b, fb, kb * kBK, n0);
-                        bulk_load(smem_addr(sm.sfa[s]), p.sfa + (static_cast<int64_t>(kb) * p.sfa_groups + mt) * 512,
-                                  512, fb);
-                        bulk_load(smem_addr(sm.sfb[s]),
-                                  p.sfb + (static_cast<int64_t>(kb) * p.sfb_groups + 2 * nt) * 512, 1024, fb);
+                        if (!TENSOR) {
+                            bulk_load(smem_addr(sm.sfa[s]),
+                                      p.sfa + (static_cast<int64_t>(kb) * p.sfa_groups + mt) * 512, 512, fb);
+                            bulk_load(smem_addr(sm.sfb[s]),
+                                      p.sfb + (static_cast<int64_t>(kb) * p.sfb_groups + 2 * nt) * 512, 1024, fb);
+                        }
                         ++n_issued;
                         ring_advance<kMxStages>(s, ph);
                     }
@@ -171,18 +179,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
-                    sf_copy(tsf, smem_addr(sm.sfa[s]));
-                    sf_copy(tsf + 4, smem_addr(sm.sfb[s]));
-                    sf_copy(tsf + 8, smem_addr(sm.sfb[s] + 512));
                     const uint64_t adesc = smem_desc_k_sw128(smem_addr(sm.a[s]));
                     const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sm.b[s]));
+                    if (TENSOR) {
 #pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k) {
-                        const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) |
-                                               (static_cast<uint32_t>(k) << 29);
-                        mma_mx(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
-                               (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kBK / 32; ++k)
+                            mma_f8f6f4(tmem_base, adesc + 2u * k, bdesc + 2u * k, p.idesc,
+                                       (kb > 0 || k > 0) ? 1u : 0u);
+                    } else {
+                        const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
+                        sf_copy(tsf, smem_addr(sm.sfa[s]));
+                        sf_copy(tsf + 4, smem_addr(sm.sfb[s]));
+                        sf_copy(tsf + 8, smem_addr(sm.sfb[s] + 512));
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k) {
+                            const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) |
+                                                   (static_cast<uint32_t>(k) << 29);
+                            mma_mx(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
+                                   (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit(smem_addr(&sm.empty[s]));
                     if (kb == nkb - 1) mma_commit(smem_addr(&sm.acc_full));
@@ -246,6 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty));
+            if (TENSOR) {
+                const float st = __fmul_rn(*p.tsa, *p.tsb);
+                const uint64_t st2 = pack_f32x2(st, st);
+#pragma unroll
+                for (int j = 0; j < 4 * kChunks; ++j) acc[j] = mul_f32x2(acc[j], st2);
+            }
             const int row0 = m0 + q * 32 + g8;
             const int col0 = n0 + half * kHalfN + 2 * cq;
             if (EPI == kEpiWgrad) {
@@ -267,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kMxTmemCols);
 }
 
-template <int EPI>
+template <int EPI, bool TENSOR>
 int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid) {
-    auto kern = gemm_mx_kernel<EPI>;
+    auto kern = gemm_mx_kernel<EPI, TENSOR>;
     static unsigned long long configured = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
@@ -285,16 +306,25 @@ int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t str
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
+template <bool TENSOR>
+int launch_family(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
     switch (epi) {
-        case kEpiNone: return launch_mx_impl<kEpiNone>(maps, p, stream, grid);
-        case kEpiBias: return launch_mx_impl<kEpiBias>(maps, p, stream, grid);
-        case kEpiBiasGelu: return launch_mx_impl<kEpiBiasGelu>(maps, p, stream, grid);
-        case kEpiDgelu: return launch_mx_impl<kEpiDgelu>(maps, p, stream, grid);
-        case kEpiDgeluBgrad: return launch_mx_impl<kEpiDgeluBgrad>(maps, p, stream, grid);
-        case kEpiWgrad: return launch_mx_impl<kEpiWgrad>(maps, p, stream, grid);
+        case kEpiNone: return launch_mx_impl<kEpiNone, TENSOR>(maps, p, stream, grid);
+        case kEpiBias: return launch_mx_impl<kEpiBias, TENSOR>(maps, p, stream, grid);
+        case kEpiBiasGelu: return launch_mx_impl<kEpiBiasGelu, TENSOR>(maps, p, stream, grid);
+        case kEpiDgelu: return launch_mx_impl<kEpiDgelu, TENSOR>(maps, p, stream, grid);
+        case kEpiDgeluBgrad: return launch_mx_impl<kEpiDgeluBgrad, TENSOR>(maps, p, stream, grid);
+        case kEpiWgrad: return launch_mx_impl<kEpiWgrad, TENSOR>(maps, p, stream, grid);
         default: return -3;
     }
+}
+
+int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
+    return launch_family<false>(maps, p, epi, stream, grid);
+}
+
+int launch_gemm_tensor(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
+    return launch_family<true>(maps, p, epi, stream, grid);
 }
 
 }  // namespace fp8ll

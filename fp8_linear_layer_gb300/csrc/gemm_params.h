@@ -48,6 +48,8 @@ struct GemmParams {
     const uint8_t* sfb;
     int64_t sfa_groups;   // MXFP8: 128-row groups per K block of each scale array
     int64_t sfb_groups;
+    const float* tsa;     // per-tensor scaling: the one fp32 scale of A and of B
+    const float* tsb;
     GroupEntry groups[kMaxGroups];
 };
 

@@ -13,6 +13,12 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
 int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
                          float* scale_rows, int64_t sld_rows, uint8_t* q_cols, float* scale_cols, int64_t sld_cols,
                          cudaStream_t stream);
+int launch_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, float* amax, cudaStream_t stream,
+                       int num_sms);
+int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
+                           uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, cudaStream_t stream,
+                           int num_sms);
+int launch_amax_history(float* hist, int64_t len, const float* amax_new, float* amax_use, cudaStream_t stream);
 int64_t mx_sf_groups(int64_t rows);
 int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
                        uint8_t* sf, cudaStream_t stream, int num_sms);
@@ -25,6 +31,7 @@ int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, int 
                       int grid);
 int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, int fast, cudaStream_t stream, int grid);
 int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
+int launch_gemm_tensor(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* bgrad, cudaStream_t stream,
                           int num_sms);
 

@@ -147,15 +147,27 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // after the loads each half-warp holds one row's 128 values in registers, so
 // the row amax (a half-warp butterfly), scale and codes need no second read
 // of x.  The arithmetic is the row kernel's, so the codes are the same.
-template <int FMT, bool ROWS>
+//
+// With TENSOR the tile is cast with the one per-tensor scale instead (from the
+// given amax: inv = fl32(FMAX/amax), scale = fl32(amax/FMAX); "FP8 GEMM for
+// the fprop should use fast accumulation" scales whole tensors): no block amax,
+// `scale` receives the single scale (written by the first CTA), sr is unused,
+// and when amax_out is given the CTA folds max|x| of its tile into it.
+template <int FMT, bool ROWS, bool TENSOR>
 __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
                                                             float* __restrict__ scale, int64_t sld,
                                                             uint8_t* __restrict__ qr, float* __restrict__ sr,
-                                                            int64_t sldr) {
+                                                            int64_t sldr, const float* __restrict__ amax_in,
+                                                            unsigned* __restrict__ amax_out) {
     __shared__ __align__(16) uint32_t tile[128][64];
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+    float inv_t = 1.0f, s_t = 1.0f;
+    if (TENSOR) {
+        block_scale<FMT>(*amax_in, inv_t, s_t);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *scale = s_t;
+    }
 
     // thread t, iteration it: row (t + 256 it) / 16 of the tile, columns
     // 8 ((t + 256 it) % 16) .. +7; all eight loads are issued first
@@ -167,6 +179,7 @@ __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* _
         v[it] = make_uint4(0, 0, 0, 0);
         if (c < cols) v[it] = __ldcs(reinterpret_cast<const uint4*>(x + (r0 + (i >> 4)) * ldx + c));
     }
+    float tmax = 0.0f;  // TENSOR: max|x| over this thread's loads
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int i = threadIdx.x + it * 256;
@@ -174,19 +187,31 @@ __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* _
         const int ch = i & 15;
         const int w = (ch * 4 + 8 * (rr >> 5)) & 63;
         *reinterpret_cast<uint4*>(&tile[rr][w]) = v[it];
-        if (ROWS) {
+        if (ROWS || (TENSOR && amax_out)) {
             const float f[8] = {bf16_lo(v[it].x), bf16_hi(v[it].x), bf16_lo(v[it].y), bf16_hi(v[it].y),
                                 bf16_lo(v[it].z), bf16_hi(v[it].z), bf16_lo(v[it].w), bf16_hi(v[it].w)};
             float amax = 0.0f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+            if (TENSOR) {
+                tmax = fmaxf(tmax, amax);
+                if (ROWS) *reinterpret_cast<uint2*>(qr + (r0 + rr) * cols + c0 + ch * 8) = encode8<FMT>(f, inv_t);
+            } else {
 #pragma unroll
-            for (int off = 1; off <= 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-            float inv, s;
-            block_scale<FMT>(amax, inv, s);
-            *reinterpret_cast<uint2*>(qr + (r0 + rr) * cols + c0 + ch * 8) = encode8<FMT>(f, inv);
-            if (ch == 0) sr[(c0 >> 7) * sldr + r0 + rr] = s;
+                for (int off = 1; off <= 8; off <<= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                float inv, s;
+                block_scale<FMT>(amax, inv, s);
+                *reinterpret_cast<uint2*>(qr + (r0 + rr) * cols + c0 + ch * 8) = encode8<FMT>(f, inv);
+                if (ch == 0) sr[(c0 >> 7) * sldr + r0 + rr] = s;
+            }
         }
+    }
+    if (TENSOR && amax_out) {
+        // non-negative floats order like their bit patterns
+#pragma unroll
+        for (int off = 1; off <= 16; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        if ((threadIdx.x & 31) == 0) atomicMax(amax_out, __float_as_uint(tmax));
     }
     __syncthreads();
 
@@ -196,21 +221,23 @@ __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* _
     // two passes over the staged tile (amax, then encode) instead of holding
     // 64 values in registers: the lower register count keeps more tiles, and
     // so more loads, in flight per SM
-    float amax_lo = 0.0f, amax_hi = 0.0f;
+    float inv_lo = inv_t, s_lo = s_t, inv_hi = inv_t, s_hi = s_t;
+    if (!TENSOR) {
+        float amax_lo = 0.0f, amax_hi = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
-        amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
-        amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
-    }
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
+            amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
+            amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
+        }
 #pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
-        amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
-        amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
+        for (int off = 1; off <= 2; off <<= 1) {
+            amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
+            amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
+        }
+        block_scale<FMT>(amax_lo, inv_lo, s_lo);
+        block_scale<FMT>(amax_hi, inv_hi, s_hi);
     }
-    float inv_lo, s_lo, inv_hi, s_hi;
-    block_scale<FMT>(amax_lo, inv_lo, s_lo);
-    block_scale<FMT>(amax_hi, inv_hi, s_hi);
     if (c < cols) {
         uint32_t wl[8], wh[8];
 #pragma unroll
@@ -232,11 +259,81 @@ __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* _
         dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
         dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-        if (p == 0) {
+        if (!TENSOR && p == 0) {
             scale[static_cast<int64_t>(blockIdx.y) * sld + c] = s_lo;
             scale[static_cast<int64_t>(blockIdx.y) * sld + c + 1] = s_hi;
         }
     }
+}
+
+// --------------------------------------------------------------- per-tensor
+// max|x| over a bf16 matrix: each warp walks rows, its lanes 16 bytes apart
+// along the row; one atomic max per warp on the bit pattern (non-negative
+// floats order like their bits), into a word the launcher zeroed first.
+__global__ void __launch_bounds__(256) tensor_amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                          int64_t cols, int64_t ldx, unsigned* __restrict__ amax) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * 8;
+    float m = 0.0f;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); r < rows; r += warps) {
+        const uint16_t* row = x + r * ldx;
+#pragma unroll 4
+        for (int64_t c = 8 * lane; c < cols; c += 256) {
+            const uint4 v = __ldcs(reinterpret_cast<const uint4*>(row + c));
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                               fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
+                               fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+        }
+    }
+#pragma unroll
+    for (int off = 1; off <= 16; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) atomicMax(amax, __float_as_uint(m));
+}
+
+// Per-tensor cast along rows: q [rows][cols] (packed), 8 codes per lane from
+// one 16-byte load, the scale from the given amax (the first thread stores it);
+// with amax_out, max|x| of the tensor is folded in as in tensor_amax_kernel.
+template <int FMT>
+__global__ void __launch_bounds__(256) tensor_quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                   int64_t cols, int64_t ldx, const float* amax_in,
+                                                                   uint8_t* __restrict__ q, float* scale,
+                                                                   unsigned* amax_out) {
+    float inv, s;
+    block_scale<FMT>(*amax_in, inv, s);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * 8;
+    float m = 0.0f;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); r < rows; r += warps) {
+        const uint16_t* row = x + r * ldx;
+#pragma unroll 4
+        for (int64_t c = 8 * lane; c < cols; c += 256) {
+            const uint4 v = __ldcs(reinterpret_cast<const uint4*>(row + c));
+            const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+            *reinterpret_cast<uint2*>(q + r * cols + c) = encode8<FMT>(f, inv);
+        }
+    }
+    if (amax_out) {
+#pragma unroll
+        for (int off = 1; off <= 16; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) atomicMax(amax_out, __float_as_uint(m));
+    }
+}
+
+// history [len] <- (amax_new, history[0 .. len-2]); *amax_use = its maximum.
+// One thread: the history is a handful of floats.
+__global__ void amax_history_kernel(float* hist, int64_t len, const float* amax_new, float* amax_use) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    const float a = *amax_new;
+    for (int64_t i = len - 1; i > 0; --i) hist[i] = hist[i - 1];
+    hist[0] = a;
+    float m = 0.0f;
+    for (int64_t i = 0; i < len; ++i) m = fmaxf(m, hist[i]);
+    *amax_use = m;
 }
 
 // -------------------------------------------------------------------- MXFP8
@@ -444,11 +541,11 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
     } else {
         dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
         if (fmt == 0)
-            quantize_cols_kernel<0, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld, nullptr,
-                                                                      nullptr, 0);
+            quantize_cols_kernel<0, false, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld,
+                                                                             nullptr, nullptr, 0, nullptr, nullptr);
         else
-            quantize_cols_kernel<1, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld, nullptr,
-                                                                      nullptr, 0);
+            quantize_cols_kernel<1, false, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld,
+                                                                             nullptr, nullptr, 0, nullptr, nullptr);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
@@ -459,11 +556,65 @@ int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx,
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
     if (fmt == 0)
-        quantize_cols_kernel<0, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols,
-                                                                 q_rows, scale_rows, sld_rows);
+        quantize_cols_kernel<0, true, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols,
+                                                                        sld_cols, q_rows, scale_rows, sld_rows,
+                                                                        nullptr, nullptr);
     else
-        quantize_cols_kernel<1, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols,
-                                                                 q_rows, scale_rows, sld_rows);
+        quantize_cols_kernel<1, true, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols,
+                                                                        sld_cols, q_rows, scale_rows, sld_rows,
+                                                                        nullptr, nullptr);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+static int grid_rows(int64_t rows, int num_sms) {
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+    return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+int launch_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, float* amax, cudaStream_t stream,
+                       int num_sms) {
+    if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return -3;
+    tensor_amax_kernel<<<grid_rows(rows, num_sms), 256, 0, stream>>>(static_cast<const uint16_t*>(x), rows, cols,
+                                                                     ldx, reinterpret_cast<unsigned*>(amax));
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
+                           uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, cudaStream_t stream,
+                           int num_sms) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    unsigned* am = reinterpret_cast<unsigned*>(amax_out);
+    if (am && cudaMemsetAsync(am, 0, sizeof(float), stream) != cudaSuccess) return -3;
+    if (q_cols) {
+        dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+        if (q_rows) {
+            if (fmt == 0)
+                quantize_cols_kernel<0, true, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale, 0,
+                                                                               q_rows, nullptr, 0, amax_in, am);
+            else
+                quantize_cols_kernel<1, true, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale, 0,
+                                                                               q_rows, nullptr, 0, amax_in, am);
+        } else {
+            if (fmt == 0)
+                quantize_cols_kernel<0, false, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale,
+                                                                                0, nullptr, nullptr, 0, amax_in, am);
+            else
+                quantize_cols_kernel<1, false, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale,
+                                                                                0, nullptr, nullptr, 0, amax_in, am);
+        }
+    } else {
+        const int g = grid_rows(rows, num_sms);
+        if (fmt == 0)
+            tensor_quantize_rows_kernel<0><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, amax_in, q_rows, scale, am);
+        else
+            tensor_quantize_rows_kernel<1><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, amax_in, q_rows, scale, am);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_amax_history(float* hist, int64_t len, const float* amax_new, float* amax_use, cudaStream_t stream) {
+    amax_history_kernel<<<1, 32, 0, stream>>>(hist, len, amax_new, amax_use);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -175,3 +175,67 @@ class MxLinearTrainStep(LinearTrainStep):
 
     # 5 casts + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
     KERNELS_PER_STEP = 9
+
+
+class TensorLinearTrainStep(LinearTrainStep):
+    """The same training step with one scale per operand tensor ("FP8 GEMM for
+    the fprop should use fast accumulation"): the GEMMs accumulate the raw fp8
+    products over all of K in the tensor core and scale once.
+
+    scaling="delayed": each of X, W, dY and dZ is cast with the largest amax of
+    its last ``history`` steps (values above it saturate) while the cast records
+    the tensor's own amax; the histories take those amaxes at the end of the
+    step.  Histories start at zero, so the first step casts with unit scales.
+    scaling="current": each tensor's own amax is taken first (a second read).
+    X is cast both ways in one read with one scale.  12 launches per step."""
+
+    def __init__(self, m: int, k: int, n: int, device="cuda", scaling: str = "delayed", history: int = 16):
+        assert m % 128 == 0 and k % 128 == 0 and scaling in ("delayed", "current")
+        self.m, self.k, self.n = m, k, n
+        self.acc_mode = B.ACC_FAST
+        self.scaling = scaling
+        dev = torch.device(device)
+        self.Xq = B.empty_tensor_scaled(m, k, B.E4M3, dev)
+        self.XTq = B.Fp8TensorScaled(torch.empty((k, m), dtype=torch.uint8, device=dev), self.Xq.scale, B.E4M3)
+        self.Wq = B.empty_tensor_scaled(n, k, B.E4M3, dev)
+        self.dYq = B.empty_tensor_scaled(m, k, B.E5M2, dev)
+        self.dZTq = B.empty_tensor_scaled(n, m, B.E5M2, dev)
+        self.Y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.Z = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.dZ = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.db = torch.empty((n,), dtype=torch.float32, device=dev)
+        self.dW = torch.zeros((n, k), dtype=torch.float32, device=dev)
+        self.ws = torch.empty((B.workspace_size(m, n) // 4,), dtype=torch.float32, device=dev)
+        # per tensor (X, W, dY, dZ): amax history, the amax to cast with, the amax seen
+        self.hist = torch.zeros((4, history), dtype=torch.float32, device=dev)
+        self.amax_use = torch.zeros((4, 1), dtype=torch.float32, device=dev)
+        self.amax_seen = torch.zeros((4, 1), dtype=torch.float32, device=dev)
+
+    def _cast(self, i, x, fmt, **kw):
+        if self.scaling == "current":
+            return [("quantize", lambda: B.tensor_amax(x, out=self.amax_use[i])),
+                    ("quantize", lambda: B.tensor_quantize(x, fmt, self.amax_use[i], **kw))]
+        return [("quantize", lambda: B.tensor_quantize(x, fmt, self.amax_use[i], amax_out=self.amax_seen[i], **kw))]
+
+    def _forward_plan(self, X, W, b):
+        return (self._cast(0, X, B.E4M3, rows=True, cols=True, out=self.Xq, out_t=self.XTq)
+                + self._cast(1, W, B.E4M3, out=self.Wq)
+                + [("gemm", lambda: B.tensor_gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, out=self.Y,
+                                                        aux=self.Z))])
+
+    def _backward_plan(self, X, dY):
+        plan = (self._cast(2, dY, B.E5M2, out=self.dYq)
+                + [("gemm", lambda: B.tensor_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ,
+                                                        bgrad=self.db, workspace=self.ws))]
+                + self._cast(3, self.dZ, B.E5M2, rows=False, cols=True, out_t=self.dZTq)
+                + [("gemm", lambda: B.tensor_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True))])
+        if self.scaling == "delayed":
+            plan += [("history", lambda i=i: B.amax_history_update(self.hist[i], self.amax_seen[i], self.amax_use[i]))
+                     for i in range(4)]
+        return plan
+
+    def input_grad(self, W):
+        raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+
+    # 4 casts + 4 amax updates (delayed) or 4 amax passes (current) + 3 GEMMs + bias-gradient finalize
+    KERNELS_PER_STEP = 12

@@ -7,6 +7,8 @@
  *
  *   fp8_quantize        bf16 -> e4m3 / e5m2 codes + block scales
  *   fp8_quantize_dual   both orientations of that cast from one read
+ *   fp8_mx_*            the MXFP8 variant (power-of-two scales per 32 values)
+ *   fp8_tensor_*        per-tensor scaling (current or delayed amax)
  *   fp8_gemm_fprop      C = A B^T with bias / tanh-GELU epilogues, bf16 out
  *   fp8_gemm_dgrad      C = A B^T times gelu'(Z), optional bias-gradient sums
  *   fp8_gemm_wgrad      fp32 out (+)= A B^T
@@ -271,6 +273,60 @@ int fp8_mx_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
                       size_t workspace_bytes, fp8ll_stream_t stream);
 int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
                       float* out, int accumulate, fp8ll_stream_t stream);
+
+/* ---- per-tensor scaling ----------------------------------------------------
+ * "FP8 GEMM for the fprop should use fast accumulation" casts whole tensors
+ * with one scale each.  The cast takes the amax to scale with from the caller:
+ * the tensor's own (fp8_tensor_amax first: "current scaling") or the largest
+ * amax of earlier steps (fp8_amax_history_update: "delayed scaling", where
+ * values above it saturate).  For a given amax A:
+ *   inv = fl32(FMAX / A); scale = fl32(A / FMAX); q = RNE-saturating fp8
+ *   encode of fl32(x * inv)
+ * (A = 0, or FMAX / A overflowing fp32: inv = scale = 1).  With one scale per
+ * operand, the GEMM accumulates the raw fp8 products over all of K in the
+ * tensor core's fp32 accumulator and multiplies once by fl32(sA * sB): no
+ * promotion inside the K loop.
+ *   q:     codes [rows][ld_q], K-contiguous, 16-byte aligned, ld_q % 16 == 0.
+ *   scale: DEVICE pointer to the operand's one fp32 scale (4-byte aligned). */
+typedef struct {
+    const uint8_t* q;
+    const float* scale;
+    int64_t ld_q;
+    int32_t fmt;
+    int32_t reserved;
+} fp8ll_tensor_operand_t;
+
+/* *amax = max|x| over a bf16 [rows][ldx] matrix (x 16-byte aligned, cols % 8
+ * == 0, ldx % 8 == 0, ldx >= cols); 0 for an empty matrix. */
+int fp8_tensor_amax(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, float* amax,
+                    fp8ll_stream_t stream);
+
+/* Per-tensor cast with the amax in *amax_in (device).  Outputs (at least one):
+ *   q_rows [rows][cols] (cols % 16 == 0), q_cols the transposed codes
+ *   [cols][rows] (rows % 128 == 0, rows / 128 <= 65535, cols % 8 == 0); both
+ *   together need cols % 128 == 0 and read x once.
+ * *scale receives the dequantization scale.  amax_out (may be NULL, must not
+ * be amax_in): receives max|x| of this x, for the history of the next step.
+ * x as in fp8_tensor_amax.  rows == 0 or cols == 0 is a no-op. */
+int fp8_tensor_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
+                        uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, fp8ll_stream_t stream);
+
+/* Delayed scaling: history[len] (device) <- (*amax_new, history[0 .. len-2]),
+ * then *amax_use = the largest entry.  len >= 1. */
+int fp8_amax_history_update(float* history, int64_t len, const float* amax_new, float* amax_use,
+                            fp8ll_stream_t stream);
+
+/* The three GEMMs of fp8_gemm_fprop / fp8_gemm_dgrad / fp8_gemm_wgrad (same
+ * shapes, epilogues, layouts and errors) on per-tensor scaled operands:
+ *   C[i][j] = fl32(sA * sB) * sum_k qA[i][k] qB[j][k]. */
+int fp8_tensor_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A,
+                          const fp8ll_tensor_operand_t* B, const void* bias_bf16, int epi, void* out_bf16,
+                          void* aux_bf16, fp8ll_stream_t stream);
+int fp8_tensor_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A,
+                          const fp8ll_tensor_operand_t* B, const void* aux_bf16, int epi, void* out_bf16, float* bgrad,
+                          void* workspace, size_t workspace_bytes, fp8ll_stream_t stream);
+int fp8_tensor_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* A,
+                          const fp8ll_tensor_operand_t* B, float* out, int accumulate, fp8ll_stream_t stream);
 
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: FP8LL_OK, or the first FP8LL_ERR_TIMEOUT recorded by a

@@ -94,6 +94,37 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.fp8_debug_starve_next_gemm(0) == E
 
 
+def test_tensor_scaling_validation(L):
+    import fp8_linear_layer_gb300 as f
+    E = f.binding.ERR_INVALID_ARG
+    vp = ctypes.c_void_p
+    fake, other = vp(0x10000), vp(0x20000)
+    # amax: misaligned result, cols % 8
+    assert L.fp8_tensor_amax(fake, 4, 128, 128, vp(0x10002), None) == E
+    assert L.fp8_tensor_amax(fake, 4, 100, 128, other, None) == E
+    # cast: no output, amax_out aliasing amax_in, rows-layout cols % 16,
+    # transposed rows % 128, both orientations with cols % 128
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, None, None, other, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, fake, None, fake, other, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 200, 200, 0, other, fake, None, other, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 100, 256, 256, 0, other, None, fake, other, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 136, 136, 0, other, fake, fake, other, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 3, other, fake, None, other, None, None) == E
+    assert L.fp8_tensor_quantize(None, 0, 256, 256, 0, None, None, None, None, None, None) == 0  # empty
+    # history: empty history
+    assert L.fp8_amax_history_update(fake, 0, other, other, None) == E
+    # GEMMs: ld_q % 16, missing scale, K % 128, dgrad workspace
+    op = f.binding.TensorOperandStruct(0x10000, 0x20000, 256, 0, 0)
+    bad = f.binding.TensorOperandStruct(0x10000, 0x20000, 200, 0, 0)
+    noscale = f.binding.TensorOperandStruct(0x10000, None, 256, 0, 0)
+    ob = ctypes.byref(op)
+    assert L.fp8_tensor_gemm_fprop(8, 8, 256, ob, ctypes.byref(bad), fake, 2, fake, fake, None) == E
+    assert L.fp8_tensor_gemm_fprop(8, 8, 256, ob, ctypes.byref(noscale), fake, 2, fake, fake, None) == E
+    assert L.fp8_tensor_gemm_fprop(8, 8, 200, ob, ob, fake, 2, fake, fake, None) == E
+    assert L.fp8_tensor_gemm_dgrad(8, 8, 256, ob, ob, fake, 4, fake, fake, fake, 4, None) == f.binding.ERR_WORKSPACE
+    assert L.fp8_tensor_gemm_wgrad(8, 8, 256, ob, ob, fake, 2, None) == E
+
+
 def test_mx_sizes_and_validation(L):
     import fp8_linear_layer_gb300 as f
     # groups of 128 rows, rounded up to an even count, 512 bytes per group and K block
