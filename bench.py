@@ -83,7 +83,7 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx"], default=None,
+    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx", "tensor"], default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
     ap.add_argument("--study-k", type=int, default=16384)
@@ -686,6 +686,74 @@ def run_mx_study(args):
     print(json.dumps(res))
 
 
+def run_tensor_study(args):
+    """The per-tensor scaled GEMMs (one scale per operand, scaled once after the
+    K loop) at the training-step shapes and on long K, and the per-tensor amax
+    and casts in GB/s of algorithmic bytes (amax: 2 read; rows: 2 read + 1
+    written; both orientations: 2 read + 2 written per element).  CUDA events
+    around 10 launches after 3 warm-ups."""
+    import torch
+    import workloads
+    import fp8_linear_layer_gb300 as fp8
+    reps = 10
+    m, k, n = args.m, args.k, args.n
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps
+
+    def cast(t, fmt, **kw):
+        return fp8.tensor_quantize(t, fmt, fp8.tensor_amax(t), **kw)
+
+    res = {"study": "tensor", "reps": reps, "tensor_tflops": {}, "cast_gbs": {}}
+    x = workloads.normal_bf16((m, k), SEED, "X").cuda()
+    w = workloads.normal_bf16((n, k), SEED, "W", std=0.02).cuda()
+    bias = workloads.normal_bf16((n,), SEED, "b", std=0.02).cuda()
+    dy = workloads.normal_bf16((m, k), SEED, "dY", std=1e-2).cuda()
+    f = 2.0 * m * n * k / 1e9
+    Y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    Z, dZ = torch.empty_like(Y), torch.empty_like(Y)
+    (X, XT), (W, _), (DY, _) = cast(x, fp8.E4M3, cols=True), cast(w, fp8.E4M3), cast(dy, fp8.E5M2)
+    res["tensor_tflops"]["fprop_bias_gelu_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.tensor_gemm_fprop(X, W, bias, fp8.EPI_BIAS_GELU, out=Y, aux=Z))
+    res["tensor_tflops"]["dgrad_dgelu_bgrad_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.tensor_gemm_dgrad(DY, W, Z, fp8.EPI_DGELU_BGRAD, out=dZ))
+    _, DZT = cast(dZ, fp8.E5M2, rows=False, cols=True)
+    dW = torch.zeros((n, k), device="cuda")
+    res["tensor_tflops"]["wgrad_accumulate_m%d_n%d_k%d" % (n, k, m)] = f / timed(
+        lambda: fp8.tensor_gemm_wgrad(DZT, XT, dW))
+    del X, XT, W, DY, DZT
+    a = workloads.normal_bf16((8192, 16384), SEED + 1, "A", std=0.02).cuda()
+    bb = workloads.normal_bf16((8192, 16384), SEED + 1, "B", std=0.02).cuda()
+    fl = 2.0 * 8192 * 8192 * 16384 / 1e9
+    o = torch.zeros((8192, 8192), device="cuda")
+    (At, _), (Bt, _) = cast(a, fp8.E4M3), cast(bb, fp8.E4M3)
+    res["tensor_tflops"]["wgrad_accumulate_m8192_n8192_k16384"] = fl / timed(lambda: fp8.tensor_gemm_wgrad(At, Bt, o))
+    del At, Bt, a, bb, o
+    xb = workloads.normal_bf16((32768, 8192), SEED + 2, "C").cuda()
+    e = xb.numel()
+    am, seen = fp8.tensor_amax(xb), torch.empty(1, device="cuda")
+    qr = fp8.empty_tensor_scaled(32768, 8192, fp8.E4M3, xb.device)
+    qt = fp8.Fp8TensorScaled(torch.empty((8192, 32768), dtype=torch.uint8, device="cuda"), qr.scale, fp8.E4M3)
+    res["cast_gbs"]["amax_32768x8192"] = e * 2.0 / 1e6 / timed(lambda: fp8.tensor_amax(xb, out=seen))
+    res["cast_gbs"]["rows_e4m3_32768x8192"] = e * 3.0 / 1e6 / timed(
+        lambda: fp8.tensor_quantize(xb, fp8.E4M3, am, out=qr, amax_out=seen))
+    res["cast_gbs"]["transposed_e4m3_32768x8192"] = e * 3.0 / 1e6 / timed(
+        lambda: fp8.tensor_quantize(xb, fp8.E4M3, am, rows=False, cols=True, out_t=qt, amax_out=seen))
+    res["cast_gbs"]["both_e4m3_32768x8192"] = e * 4.0 / 1e6 / timed(
+        lambda: fp8.tensor_quantize(xb, fp8.E4M3, am, cols=True, out=qr, out_t=qt, amax_out=seen))
+    res["status"] = fp8.device_status()
+    print(json.dumps(res))
+
+
 def run_fp8_peak_probe(args):
     """Dense fp8 tensor-core throughput of the vendor library on this GPU, for
     context beside the roofline denominator (which stays the measured bf16
@@ -747,6 +815,8 @@ def main():
         return run_wgrad_tables(args)
     if args.study == "mx":
         return run_mx_study(args)
+    if args.study == "tensor":
+        return run_tensor_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -207,13 +207,21 @@ __global__ void __launch_bounds__(256, 4) quantize_cols_kernel(const uint16_t* _
             }
         }
     }
+    __shared__ float warp_max[8];
     if (TENSOR && amax_out) {
-        // non-negative floats order like their bit patterns
 #pragma unroll
         for (int off = 1; off <= 16; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-        if ((threadIdx.x & 31) == 0) atomicMax(amax_out, __float_as_uint(tmax));
+        if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = tmax;
     }
     __syncthreads();
+    if (TENSOR && amax_out && threadIdx.x == 0) {
+        // one atomic per CTA (thousands of CTAs finish together); non-negative
+        // floats order like their bit patterns
+        float m = warp_max[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) m = fmaxf(m, warp_max[i]);
+        atomicMax(amax_out, __float_as_uint(m));
+    }
 
     const int cp = threadIdx.x >> 2;  // column pair 0..63
     const int p = threadIdx.x & 3;    // 32-row part
