@@ -147,9 +147,42 @@ __device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
 
 // wgrad: out (+)= acc, fp32.  out += acc is a single fp32 add per element,
 // done in L2 by a vector reduction (no load round trip; each element receives
-// exactly one add per call, so the result is deterministic).
+// exactly one add per call, so the result is deterministic).  16-byte
+// reductions when rows are 16-byte aligned, 8-byte ones otherwise.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, int row0, int col0,
                                             const uint64_t (&acc)[4 * kChunks]) {
+    if ((p.N & 3) == 0) {
+        // rows 16-byte aligned: neighbouring lanes of a quad swap one column
+        // pair so that each holds four consecutive columns of one chunk of a
+        // chunk pair (even lane: the first chunk, odd lane: the second) and
+        // adds them with one 16-byte reduction
+        const int cq = (col0 >> 1) & 3;
+        const bool odd = (cq & 1) != 0;
+        const int cb = col0 - 2 * (cq & 1);  // first column of the lane pair
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + 8 * r;
+            float* orow = static_cast<float*>(p.out) + (static_cast<int64_t>(out_index) * p.M + row) * p.N;
+#pragma unroll
+            for (int c = 0; c < kChunks; c += 2) {
+                const uint64_t mine = odd ? acc[4 * (c + 1) + r] : acc[4 * c + r];
+                const uint64_t recv = __shfl_xor_sync(0xffffffffu, odd ? acc[4 * c + r] : acc[4 * (c + 1) + r], 1);
+                const float2 lo = unpack_f32x2(odd ? recv : mine), hi = unpack_f32x2(odd ? mine : recv);
+                const int col = cb + 8 * (c + (odd ? 1 : 0));
+                if (row >= p.M || col >= p.N) continue;
+                if (p.accumulate)
+                    red_add_v4(orow + col, lo.x, lo.y, hi.x, hi.y);
+                else
+                    *reinterpret_cast<float4*>(orow + col) = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+        return;
+    }
     const bool pairs = (p.N & 1) == 0;  // column pairs are 8-byte aligned
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -172,6 +205,30 @@ __device__ __forceinline__ void store_wgrad(const GemmParams& p, int out_index, 
                 if (col + 1 < p.N) orow[col + 1] = (p.accumulate ? orow[col + 1] : 0.0f) + v.y;
             }
         }
+    }
+}
+
+// 4 x 4 transpose of 32-bit words among the four lanes of a quad (lanes that
+// differ in bits 0-1): on entry a[j] is this lane's word j; on exit a[j] is
+// word (lane % 4) of lane j.  Two butterfly stages, two shuffles each.
+__device__ __forceinline__ void quad_transpose(uint32_t (&a)[4], int cq) {
+    const bool odd = (cq & 1) != 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? a[2 * q] : a[2 * q + 1], 1);
+        if (odd)
+            a[2 * q] = recv;
+        else
+            a[2 * q + 1] = recv;
+    }
+    const bool hi = (cq & 2) != 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? a[j] : a[2 + j], 2);
+        if (hi)
+            a[j] = recv;
+        else
+            a[2 + j] = recv;
     }
 }
 
@@ -199,6 +256,44 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int c
                 bw[c] = static_cast<uint32_t>(bias[col]) |
                         (col + 1 < p.N ? static_cast<uint32_t>(bias[col + 1]) << 16 : 0u);
         }
+    }
+    if ((p.N & 7) == 0) {
+        // rows 16-byte aligned: the quad's four lanes swap words so that each
+        // holds eight consecutive columns of one chunk and stores them as one
+        // 16-byte vector (a warp store then covers 64 contiguous bytes of each
+        // of its eight rows)
+        const int cq = (col0 >> 1) & 3;
+        const int cbase = col0 - 2 * cq;
+#pragma unroll
+        for (int g = 0; g < kChunks / 4; ++g) {
+            uint32_t yw[4][4], zw[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 4 * g + j;
+                const float b0 = bf16_lo(bw[c]), b1 = bf16_hi(bw[c]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float2 a = unpack_f32x2(acc[4 * c + r]);
+                    const float z0 = a.x + b0, z1 = a.y + b1;
+                    const float y0 = (EPI == kEpiBiasGelu) ? gelu_tanh(z0) : z0;
+                    const float y1 = (EPI == kEpiBiasGelu) ? gelu_tanh(z1) : z1;
+                    yw[r][j] = pack_bf16x2(y0, y1);
+                    zw[r][j] = pack_bf16x2(z0, z1);
+                }
+            }
+            const int col = cbase + 8 * (4 * g + cq);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                quad_transpose(yw[r], cq);
+                if (aux) quad_transpose(zw[r], cq);
+                const int row = row0 + 8 * r;
+                if (row >= p.M || col >= p.N) continue;
+                const int64_t off = static_cast<int64_t>(row) * p.N + col;
+                *reinterpret_cast<uint4*>(out + off) = make_uint4(yw[r][0], yw[r][1], yw[r][2], yw[r][3]);
+                if (aux) *reinterpret_cast<uint4*>(aux + off) = make_uint4(zw[r][0], zw[r][1], zw[r][2], zw[r][3]);
+            }
+        }
+        return;
     }
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
