@@ -334,7 +334,11 @@ __device__ __forceinline__ void store_fprop(const GemmParams& p, int row0, int c
 // column (zero outside the matrix) is summed over the warp's 32 rows -- the
 // thread's four rows first, then across the eight lanes that hold the same
 // columns (lane xor 4, 8, 16), a fixed order, so results are deterministic --
-// and lanes 0..3 write the chunk's eight sums to the workspace band of this warp.
+// and the sums go to the workspace band of this warp.  The cross-lane step is
+// a reduce-scatter after the last chunk: each of its three stages keeps half
+// of the thread's (chunk, column) sums and adds the partner lane's copy of
+// them (28 shuffles per thread instead of 96 for a butterfly per chunk), and
+// every lane ends with four finished sums to store.
 //
 // The stored pre-activations come from one of two places.  ZSMEM: the tile's
 // Z was staged in shared memory by TMA (zs = the 128 x 256 tile as four
@@ -386,6 +390,7 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
     uint16_t* out = static_cast<uint16_t*>(p.out);
     const uint16_t* zp = static_cast<const uint16_t*>(p.aux);
     const int g8 = lane >> 2;
+    float cs[2 * kChunks];  // BGRAD: column sums over the thread's four rows, per (chunk, column)
     uint32_t zcur[4 * kZGroup], znext[4 * kZGroup];
     if (!ZSMEM) load_z_group(p, zp, pairs, row0, col0, 0, zcur);
 #pragma unroll
@@ -424,21 +429,34 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
                     if (two) out[off + 1] = static_cast<uint16_t>(pack_bf16x2(d[r][1], 0.0f) & 0xFFFFu);
                 }
             }
-            if (BGRAD) {
-#pragma unroll
-                for (int m = 4; m <= 16; m <<= 1) {
-                    s0 += __shfl_xor_sync(0xffffffffu, s0, m);
-                    s1 += __shfl_xor_sync(0xffffffffu, s1, m);
-                }
-                if (lane < 4) {
-                    if (one) band[col] = s0;
-                    if (two) band[col + 1] = s1;
-                }
-            }
+            cs[2 * c] = s0;
+            cs[2 * c + 1] = s1;
         }
         if (!ZSMEM && c0 + kZGroup < kChunks) {
 #pragma unroll
             for (int j = 0; j < 4 * kZGroup; ++j) zcur[j] = znext[j];
+        }
+    }
+    if (BGRAD) {
+        int lo = 0;  // first (chunk, column) index this lane still holds
+#pragma unroll
+        for (int st = 0; st < 3; ++st) {
+            const int half = kChunks >> st;  // the lane holds 2 * half sums before the stage
+            const bool upper = ((g8 >> st) & 1) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float keep = upper ? cs[half + i] : cs[i];
+                const float give = upper ? cs[i] : cs[half + i];
+                cs[i] = keep + __shfl_xor_sync(0xffffffffu, give, 4 << st);
+            }
+            lo += upper ? half : 0;
+        }
+        // (chunk, column) indices lo .. lo + 3: chunks lo / 2 and lo / 2 + 1
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int v = lo + i;
+            const int col = col0 + 8 * (v >> 1) + (v & 1);
+            if (col < p.N) band[col] = cs[i];
         }
     }
 }
