@@ -49,9 +49,40 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_mutant(name, tmp_path):
-    old, new = MUTANTS[name]
+# per-tensor scaling: checked against its own pin file only
+TENSOR_MUTANTS = {
+    "tensor cast scale inverted": ("scale = amax_in / fmax; /* binary32 division */",
+                                   "scale = fmax / amax_in; /* binary32 division */"),
+    "tensor cast ignores the given amax": ("const float t = fmax / amax_in; /* binary32 division */",
+                                           "const float t = fmax / 1.0f; /* binary32 division */"),
+    "tensor cast records a signed maximum": ("const float a = fabsf(v);\n            if (a > amax) amax = a;",
+                                             "const float a = v;\n            if (a > amax) amax = a;"),
+    "tensor cast transposes wrongly": ("q[c * rows + r] = code;", "q[r * cols + c] = code;"),
+    "history keeps the oldest instead of the newest": ("    hist[0] = amax_new;\n", "    hist[0] = hist[0];\n"),
+    "history maximum skips the newest": ("for (int64_t i = 0; i < len; ++i)\n        if (hist[i] > m) m = hist[i];",
+                                         "for (int64_t i = 1; i < len; ++i)\n        if (hist[i] > m) m = hist[i];"),
+    "tensor gemm drops the B scale": ("const double s = (double)sa * (double)sb;", "const double s = (double)sa;"),
+    "tensor gemm reads a wrong B row": ("const double p = ta[qa[i * lda + k]] * tb[qb[j * ldb + k]];",
+                                        "const double p = ta[qa[i * lda + k]] * tb[qb[(j % 3) * ldb + k]];"),
+}
+
+
+# MXFP8: checked against its own pin file only
+MX_MUTANTS = {
+    "mx exponent one too small (the block saturates)": (
+        "while (e > -127 && amax <= ldexp(fmax, e - 1)) --e;", "while (e > -127 && amax < ldexp(fmax, e)) --e;"),
+    "mx codes scaled by 2^e instead of 2^-e": ("oracle_fp8_encode(fmt, (float)ldexp((double)v[k], -e));",
+                                               "oracle_fp8_encode(fmt, (float)ldexp((double)v[k], e));"),
+    "mx transposed cast reads rows": ("v[k] = oracle_bf16_to_f32(x[(b * 32 + k) * ldx + c]);",
+                                      "v[k] = oracle_bf16_to_f32(x[(b * 32 + k) * ldx + (c % 2)]);"),
+    "mx gemm drops the B exponent": ("const double b = ldexp(tb[qb[j * ldb + k]], eb[(k / 32) * eb_ld + j]);",
+                                     "const double b = tb[qb[j * ldb + k]];"),
+    "mx gemm uses the wrong 32-element group": ("const double a = ldexp(ta[qa[i * lda + k]], ea[(k / 32) * ea_ld + i]);",
+                                                "const double a = ldexp(ta[qa[i * lda + k]], ea[(k / 128) * ea_ld + i]);"),
+}
+
+
+def run_pins_on_mutant(tmp_path, old, new, name, pin_tests):
     text = open(SRC).read()
     assert text.count(old) == 1, "mutation anchor not found: %s" % name
     src = tmp_path / "oracle.c"
@@ -61,6 +92,24 @@ def test_pins_catch_mutant(name, tmp_path):
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
                            "-o", str(lib), str(src), "-lm"])
     env = dict(os.environ, ORACLE_LIB=str(lib))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] + PIN_TESTS,
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] + pin_tests,
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "pins did not catch: %s\n%s" % (name, r.stdout[-2000:])
+
+
+@pytest.mark.parametrize("name", sorted(TENSOR_MUTANTS))
+def test_tensor_pins_catch_mutant(name, tmp_path):
+    old, new = TENSOR_MUTANTS[name]
+    run_pins_on_mutant(tmp_path, old, new, name, ["tests/test_oracle_tensor.py"])
+
+
+@pytest.mark.parametrize("name", sorted(MX_MUTANTS))
+def test_mx_pins_catch_mutant(name, tmp_path):
+    old, new = MX_MUTANTS[name]
+    run_pins_on_mutant(tmp_path, old, new, name, ["tests/test_oracle_mx.py"])
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    run_pins_on_mutant(tmp_path, old, new, name, PIN_TESTS)

@@ -127,3 +127,13 @@ def test_tensor_gemm_closed_form_and_float64_matmul(oracle_mod):
     # a transposed operand gives the transposed result
     acc_t, _ = oracle_mod.tensor_gemm(qb, sb, E5M2, qa, sa, E4M3)
     assert np.allclose(acc_t, acc.T, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_recorded_amax_is_a_magnitude(oracle_mod):
+    # the largest magnitude is negative: the recorded amax is its absolute value
+    x = torch.full((2, 128), 0.5, dtype=torch.float32)
+    x[1, 77] = -9.0
+    x[0, 3] = 4.0
+    q, s, a = oracle_mod.tensor_quantize(workloads.bits(x.to(torch.bfloat16)), E4M3, 9.0)
+    assert a == 9.0
+    assert q[1, 77] == 0xFE and s == np.float32(9.0) / np.float32(448.0)
