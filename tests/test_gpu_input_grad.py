@@ -37,7 +37,7 @@ def test_input_grad_vs_oracle(fp8, m, k, n):
 
 
 def test_train_step_input_grad_matches_direct_call(fp8):
-    # the driver's dX is the same GEMM on the same casts: bit-identical
+    # the training step's dX is the same GEMM on the same casts: bit-identical
     from fp8_linear_layer_gb300.linear import LinearTrainStep
     m, k, n = 256, 384, 512
     X = workloads.normal_bf16((m, k), 72, "x").cuda()
