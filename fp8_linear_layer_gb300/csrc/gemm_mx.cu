@@ -23,7 +23,8 @@
 // TENSOR = true is the per-tensor scaled GEMM ("FP8 GEMM for the fprop should
 // use fast accumulation": one scale per operand tensor): no scale atoms, plain
 // kind::f8f6f4 MMAs accumulate the raw fp8 products over the whole K range in
-// the same TMEM accumulator, and the epilogue multiplies the fp32 sums by
+// one of two TMEM accumulators (alternating per tile: without scale slots the
+// 512 columns hold two), and the epilogue multiplies the fp32 sums by
 // fl32(sA * sB) once -- no promotion inside the K loop.
 #include "gemm_kernel.cuh"
 
@@ -43,8 +44,8 @@ struct __align__(1024) MxSmem {
     uint8_t sfb[kMxStages][1024];
     uint64_t full[kMxStages];
     uint64_t empty[kMxStages];
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t acc_full[2];  // one accumulator (MXFP8) or two (per-tensor)
+    uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
 };
@@ -88,14 +89,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t budget = p.budget_ns;
     const int nkb = p.groups[0].nkb;
+    // per-tensor: two 256-column accumulators, so a tile's MMAs do not wait for
+    // the epilogue to read the previous tile; MXFP8 needs columns 256.. for scales
+    constexpr int kAccBufs = TENSOR ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMxStages; ++s) {
             mbar_init(smem_addr(&sm.full[s]), 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
-        mbar_init(smem_addr(&sm.acc_full), 1);
-        mbar_init(smem_addr(&sm.acc_empty), kEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&sm.acc_full[b]), 1);
+            mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
+        }
         mbar_init(smem_addr(&sm.drain), 1);
         fence_mbar_init();
     }
@@ -164,16 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
-        int s = 0;
+        int s = 0, ab = 0;
         uint32_t ph = 0, aph = 0;
         uint32_t slot = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-            // the accumulator must have been read by the epilogue of the previous tile
-            ok = warp_all(mbar_wait(smem_addr(&sm.acc_empty), aph ^ 1u, budget));
+            // the accumulator must have been read by the epilogue of the tile that used it last
+            ok = warp_all(mbar_wait(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget));
             if (!ok) break;
-            aph ^= 1u;
             tc_fence_after();
+            const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * kBN);
             for (int kb = 0; kb < nkb; ++kb) {
                 ok = warp_all(mbar_wait(smem_addr(&sm.full[s]), ph, budget));
                 if (!ok) break;
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (TENSOR) {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
-                            mma_f8f6f4(tmem_base, adesc + 2u * k, bdesc + 2u * k, p.idesc,
+                            mma_f8f6f4(dacc, adesc + 2u * k, bdesc + 2u * k, p.idesc,
                                        (kb > 0 || k > 0) ? 1u : 0u);
                     } else {
                         const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
@@ -195,17 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < kBK / 32; ++k) {
                             const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) |
                                                    (static_cast<uint32_t>(k) << 29);
-                            mma_mx(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
+                            mma_mx(dacc, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
                                    (kb > 0 || k > 0) ? 1u : 0u);
                         }
                     }
                     mma_commit(smem_addr(&sm.empty[s]));
-                    if (kb == nkb - 1) mma_commit(smem_addr(&sm.acc_full));
+                    if (kb == nkb - 1) mma_commit(smem_addr(&sm.acc_full[ab]));
                 }
                 __syncwarp();
                 ring_advance<kMxStages>(s, ph);
                 slot = (slot + 1) % kMxSfSlots;
             }
+            ring_advance<kAccBufs>(ab, aph);
         }
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
         if (lane == 0) mma_commit(smem_addr(&sm.drain));
@@ -220,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;
         const int g8 = lane >> 2;
         const int cq = lane & 3;
+        int ab = 0;
         uint32_t aph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
@@ -237,13 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     prefetch_l2(zrow + pc1);
                 }
             }
-            ok = warp_all(mbar_wait(smem_addr(&sm.acc_full), aph, budget));
+            ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
             if (!ok) break;
-            aph ^= 1u;
             tc_fence_after();
             uint64_t acc[4 * kChunks];
             const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>(half * kHalfN);
+                                static_cast<uint32_t>(ab * kBN + half * kHalfN);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 uint64_t plo[8], phi[8];
@@ -260,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the tile's sums are in registers: the accumulator goes back to the MMA warp
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty));
+            if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+            ring_advance<kAccBufs>(ab, aph);
             if (TENSOR) {
                 const float st = __fmul_rn(*p.tsa, *p.tsb);
                 const uint64_t st2 = pack_f32x2(st, st);
