@@ -245,3 +245,48 @@ def test_delayed_scaling_training_step(fp8):
     acc2, S2 = oracle.tensor_gemm(qdz, sdz, E5M2, qxt, sxt, E4M3)
     inc = (st.dW - dW1).cpu().double().numpy()
     assert_within(inc, acc2, FULL_C * S2 + 2 * f32_ulp(st.dW.cpu().double().numpy()), "dW increment")
+
+
+def test_current_scaling_training_step(fp8):
+    # current scaling: every cast takes its own tensor's amax first, so one
+    # step's forward equals the oracle with per-tensor amaxes of its inputs
+    from fp8_linear_layer_gb300.linear import TensorLinearTrainStep
+    m, k, n = 384, 256, 640
+    X = workloads.normal_bf16((m, k), 600, "X")
+    W = workloads.normal_bf16((n, k), 600, "W", std=0.05)
+    b = workloads.normal_bf16((n,), 600, "b", std=0.02)
+    dY = workloads.normal_bf16((m, k), 600, "dY", std=1e-2)
+    st = TensorLinearTrainStep(m, k, n, scaling="current")
+    st.step(X.cuda(), W.cuda(), b.cuda(), dY.cuda())
+    torch.cuda.synchronize()
+    assert fp8.device_status() == 0
+    am = [float(np.abs(t.float().numpy()).max()) for t in (X, W, dY)] + [float(st.dZ.abs().max())]
+    assert np.array_equal(st.amax_use.cpu().numpy().ravel(), np.float32(am))
+    qx, sx, _ = oracle.tensor_quantize(workloads.bits(X), E4M3, am[0])
+    qw, sw, _ = oracle.tensor_quantize(workloads.bits(W), E4M3, am[1])
+    acc, S = oracle.tensor_gemm(qx, sx, E4M3, qw, sw, E4M3)
+    Zo, Yo = oracle.fprop_epilogue(acc, workloads.bits(b))
+    y = bf16_to_f64(st.Y)
+    assert_within(y, Yo, MAX_DGELU * FULL_C * S + bf16_ulp(np.maximum(np.abs(y), np.abs(Yo))) + 1e-5 * np.abs(Zo), "Y")
+    qdz, sdz, _ = oracle.tensor_quantize(workloads.bits(st.dZ.cpu()), E5M2, am[3], transpose=True)
+    assert np.array_equal(st.dZTq.q.cpu().numpy(), qdz)
+
+
+def test_training_step_bitwise_repeatable(fp8):
+    # the amax reductions are maxima (order-free) and every GEMM sum has a
+    # fixed order: two fresh steps on the same inputs agree bit for bit
+    from fp8_linear_layer_gb300.linear import TensorLinearTrainStep
+    m, k, n = 512, 384, 768
+    X = workloads.normal_bf16((m, k), 610, "X").cuda()
+    W = workloads.normal_bf16((n, k), 610, "W", std=0.05).cuda()
+    b = workloads.normal_bf16((n,), 610, "b", std=0.02).cuda()
+    dY = workloads.normal_bf16((m, k), 610, "dY", std=1e-2).cuda()
+    outs = []
+    for _ in range(2):
+        st = TensorLinearTrainStep(m, k, n, scaling="delayed", history=3)
+        for _ in range(2):
+            st.step(X, W, b, dY)
+        outs.append([t.clone() for t in (st.Y, st.Z, st.dZ, st.db, st.dW, st.hist, st.amax_use)])
+    torch.cuda.synchronize()
+    for a, c in zip(*outs):
+        assert torch.equal(a, c)
