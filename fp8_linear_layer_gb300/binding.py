@@ -89,7 +89,7 @@ def lib():
         top = ctypes.POINTER(TensorOperandStruct)
         L.fp8_tensor_amax.argtypes = [vp, i64, i64, i64, vp, vp]
         L.fp8_tensor_quantize.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp]
-        L.fp8_amax_history_update.argtypes = [vp, i64, vp, vp, vp]
+        L.fp8_amax_history_update.argtypes = [vp, i64, i64, vp, vp, vp]
         L.fp8_tensor_gemm_fprop.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp]
         L.fp8_tensor_gemm_dgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp, sz, vp]
         L.fp8_tensor_gemm_wgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp]
@@ -416,11 +416,15 @@ def tensor_quantize(x: torch.Tensor, fmt: int, amax_in: torch.Tensor, rows: bool
 
 
 def amax_history_update(history: torch.Tensor, amax_new: torch.Tensor, amax_use: torch.Tensor) -> torch.Tensor:
-    """Delayed scaling: push amax_new into history (fp32 device tensors) and
-    write the largest entry to amax_use."""
+    """Delayed scaling: push amax_new into history and write the largest entry
+    to amax_use (fp32 device tensors).  history [len] for one tensor, or
+    [count][len] with amax_new and amax_use holding count values."""
     assert history.dtype == torch.float32 and history.is_contiguous()
-    _check(lib().fp8_amax_history_update(_ptr(history), history.numel(), _ptr(amax_new), _ptr(amax_use), _stream()),
-           "fp8_amax_history_update")
+    count = 1 if history.dim() == 1 else history.shape[0]
+    assert amax_new.numel() == count and amax_use.numel() == count
+    assert amax_new.is_contiguous() and amax_use.is_contiguous()
+    _check(lib().fp8_amax_history_update(_ptr(history), count, history.shape[-1], _ptr(amax_new), _ptr(amax_use),
+                                         _stream()), "fp8_amax_history_update")
     return amax_use
 
 

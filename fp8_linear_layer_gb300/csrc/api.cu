@@ -638,13 +638,15 @@ int fp8_tensor_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
                : FP8LL_ERR_LAUNCH;
 }
 
-int fp8_amax_history_update(float* history, int64_t len, const float* amax_new, float* amax_use,
+int fp8_amax_history_update(float* history, int64_t count, int64_t len, const float* amax_new, float* amax_use,
                             fp8ll_stream_t stream) {
-    if (!history || len < 1 || len > (1 << 20) || !amax_new || !amax_use) return FP8LL_ERR_INVALID_ARG;
+    if (!history || count < 1 || count > (1 << 20) || len < 1 || len > (1 << 20) || !amax_new || !amax_use)
+        return FP8LL_ERR_INVALID_ARG;
     DeviceInfo* dev = nullptr;
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
-    return launch_amax_history(history, len, amax_new, amax_use, reinterpret_cast<cudaStream_t>(stream)) == 0
+    return launch_amax_history(history, count, len, amax_new, amax_use, reinterpret_cast<cudaStream_t>(stream)) ==
+                   0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }

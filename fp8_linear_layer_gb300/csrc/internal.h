@@ -18,7 +18,8 @@ int launch_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, f
 int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
                            uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, cudaStream_t stream,
                            int num_sms);
-int launch_amax_history(float* hist, int64_t len, const float* amax_new, float* amax_use, cudaStream_t stream);
+int launch_amax_history(float* hist, int64_t count, int64_t len, const float* amax_new, float* amax_use,
+                        cudaStream_t stream);
 int64_t mx_sf_groups(int64_t rows);
 int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
                        uint8_t* sf, cudaStream_t stream, int num_sms);

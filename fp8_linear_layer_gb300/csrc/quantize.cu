@@ -332,16 +332,20 @@ __global__ void __launch_bounds__(256) tensor_quantize_rows_kernel(const uint16_
     }
 }
 
-// history [len] <- (amax_new, history[0 .. len-2]); *amax_use = its maximum.
-// One thread: the history is a handful of floats.
-__global__ void amax_history_kernel(float* hist, int64_t len, const float* amax_new, float* amax_use) {
-    if (blockIdx.x != 0 || threadIdx.x != 0) return;
-    const float a = *amax_new;
-    for (int64_t i = len - 1; i > 0; --i) hist[i] = hist[i - 1];
-    hist[0] = a;
+// For each of `count` histories h: history[h][len] <- (amax_new[h],
+// history[h][0 .. len-2]) and amax_use[h] = its maximum.  One thread per
+// history: each holds a handful of floats.
+__global__ void amax_history_kernel(float* hist, int64_t count, int64_t len, const float* amax_new,
+                                    float* amax_use) {
+    const int64_t h = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (h >= count) return;
+    float* row = hist + h * len;
+    const float a = amax_new[h];
+    for (int64_t i = len - 1; i > 0; --i) row[i] = row[i - 1];
+    row[0] = a;
     float m = 0.0f;
-    for (int64_t i = 0; i < len; ++i) m = fmaxf(m, hist[i]);
-    *amax_use = m;
+    for (int64_t i = 0; i < len; ++i) m = fmaxf(m, row[i]);
+    amax_use[h] = m;
 }
 
 // -------------------------------------------------------------------- MXFP8
@@ -621,8 +625,10 @@ int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-int launch_amax_history(float* hist, int64_t len, const float* amax_new, float* amax_use, cudaStream_t stream) {
-    amax_history_kernel<<<1, 32, 0, stream>>>(hist, len, amax_new, amax_use);
+int launch_amax_history(float* hist, int64_t count, int64_t len, const float* amax_new, float* amax_use,
+                        cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>((count + 127) / 128);
+    amax_history_kernel<<<blocks, 128, 0, stream>>>(hist, count, len, amax_new, amax_use);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

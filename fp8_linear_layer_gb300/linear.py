@@ -187,7 +187,9 @@ class TensorLinearTrainStep(LinearTrainStep):
     the tensor's own amax; the histories take those amaxes at the end of the
     step.  Histories start at zero, so the first step casts with unit scales.
     scaling="current": each tensor's own amax is taken first (a second read).
-    X is cast both ways in one read with one scale.  12 launches per step."""
+    X is cast both ways in one read with one scale.  9 launches per step
+    (delayed: one amax-history update for all four tensors), 12 with current
+    scaling (four amax passes)."""
 
     def __init__(self, m: int, k: int, n: int, device="cuda", scaling: str = "delayed", history: int = 16):
         assert m % 128 == 0 and k % 128 == 0 and scaling in ("delayed", "current")
@@ -230,12 +232,13 @@ class TensorLinearTrainStep(LinearTrainStep):
                 + self._cast(3, self.dZ, B.E5M2, rows=False, cols=True, out_t=self.dZTq)
                 + [("gemm", lambda: B.tensor_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True))])
         if self.scaling == "delayed":
-            plan += [("history", lambda i=i: B.amax_history_update(self.hist[i], self.amax_seen[i], self.amax_use[i]))
-                     for i in range(4)]
+            plan.append(("history", lambda: B.amax_history_update(self.hist, self.amax_seen, self.amax_use)))
         return plan
 
     def input_grad(self, W):
         raise NotImplementedError("the input gradient is built for the 1x128 recipe")
 
-    # 4 casts + 4 amax updates (delayed) or 4 amax passes (current) + 3 GEMMs + bias-gradient finalize
-    KERNELS_PER_STEP = 12
+    # 4 casts + 3 GEMMs + bias-gradient finalize + 1 history update (delayed)
+    @property
+    def KERNELS_PER_STEP(self):
+        return 9 if self.scaling == "delayed" else 12

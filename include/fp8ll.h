@@ -311,9 +311,10 @@ int fp8_tensor_amax(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx,
 int fp8_tensor_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
                         uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, fp8ll_stream_t stream);
 
-/* Delayed scaling: history[len] (device) <- (*amax_new, history[0 .. len-2]),
- * then *amax_use = the largest entry.  len >= 1. */
-int fp8_amax_history_update(float* history, int64_t len, const float* amax_new, float* amax_use,
+/* Delayed scaling, for `count` tensors at once (device pointers): history
+ * [count][len] row h <- (amax_new[h], history[h][0 .. len-2]), then
+ * amax_use[h] = the largest entry of row h.  count >= 1, len >= 1. */
+int fp8_amax_history_update(float* history, int64_t count, int64_t len, const float* amax_new, float* amax_use,
                             fp8ll_stream_t stream);
 
 /* The three GEMMs of fp8_gemm_fprop / fp8_gemm_dgrad / fp8_gemm_wgrad (same

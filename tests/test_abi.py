@@ -112,7 +112,8 @@ def test_tensor_scaling_validation(L):
     assert L.fp8_tensor_quantize(fake, 128, 256, 256, 3, other, fake, None, other, None, None) == E
     assert L.fp8_tensor_quantize(None, 0, 256, 256, 0, None, None, None, None, None, None) == 0  # empty
     # history: empty history
-    assert L.fp8_amax_history_update(fake, 0, other, other, None) == E
+    assert L.fp8_amax_history_update(fake, 1, 0, other, other, None) == E
+    assert L.fp8_amax_history_update(fake, 0, 4, other, other, None) == E
     # GEMMs: ld_q % 16, missing scale, K % 128, dgrad workspace
     op = f.binding.TensorOperandStruct(0x10000, 0x20000, 256, 0, 0)
     bad = f.binding.TensorOperandStruct(0x10000, 0x20000, 200, 0, 0)

@@ -290,3 +290,18 @@ def test_training_step_bitwise_repeatable(fp8):
     torch.cuda.synchronize()
     for a, c in zip(*outs):
         assert torch.equal(a, c)
+
+
+def test_amax_histories_batched(fp8):
+    # three histories in one call: each row behaves as the oracle's single history
+    hist = torch.zeros((3, 4), device="cuda")
+    use = torch.empty((3, 1), device="cuda")
+    h_o = [np.zeros(4, dtype=np.float32) for _ in range(3)]
+    steps = [(1.0, 5.0, 0.25), (2.0, 0.5, 0.125), (0.5, 0.25, 8.0), (0.25, 0.125, 0.5), (0.125, 4.0, 0.25)]
+    for vals in steps:
+        new = torch.tensor(vals, dtype=torch.float32, device="cuda").reshape(3, 1)
+        fp8.amax_history_update(hist, new, use)
+        torch.cuda.synchronize()
+        for h in range(3):
+            h_o[h], u = oracle.amax_history(h_o[h], vals[h])
+            assert np.array_equal(hist[h].cpu().numpy(), h_o[h]) and use[h].item() == u
