@@ -39,6 +39,7 @@ class LinearTrainStep:
         self.m, self.k, self.n = m, k, n
         self.acc_mode = acc_mode
         self.with_input_grad = input_grad
+        self.weight_cached = False
         dev = torch.device(device)
         self.Xq = B.empty_fp8(m, k, B.E4M3, dev)
         self.Wq = B.empty_fp8(n, k, B.E4M3, dev)
@@ -67,17 +68,32 @@ class LinearTrainStep:
 
     # the step as a list of (kind, launch) pairs: forward, backward and the
     # benchmark all run these
-    def _forward_plan(self, X, W, b):
+    def _weight_cast(self, W):
         if self.with_input_grad:
-            cast_w = ("quantize", lambda: B.quantize_dual(W, B.E4M3, out=self.Wq, out_t=self.WTq))
-        else:
-            cast_w = ("quantize", lambda: B.quantize(W, B.E4M3, out=self.Wq))
-        return [
-            ("quantize", lambda: B.quantize_dual(X, B.E4M3, out=self.Xq, out_t=self.XTq)),
-            cast_w,
-            ("gemm", lambda: B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y,
-                                          aux=self.Z)),
-        ]
+            return ("quantize", lambda: B.quantize_dual(W, B.E4M3, out=self.Wq, out_t=self.WTq))
+        return ("quantize", lambda: B.quantize(W, B.E4M3, out=self.Wq))
+
+    def cache_weight(self, W):
+        """Cast W now and keep its fp8 copy for the following steps, which then
+        skip the weight cast (W must not change meanwhile, e.g. while gradients
+        of several micro-batches accumulate); the copy the step casts anyway is
+        the one reused between the forward and the data-gradient GEMMs.  Caching
+        the low-precision weight across calls is the optimization "How can we
+        use te.Linear with weight parallel?" asks for."""
+        self._weight_cast(W)[1]()
+        self.weight_cached = True
+
+    def uncache_weight(self):
+        """Go back to casting W in every step."""
+        self.weight_cached = False
+
+    def _forward_plan(self, X, W, b):
+        plan = [("quantize", lambda: B.quantize_dual(X, B.E4M3, out=self.Xq, out_t=self.XTq))]
+        if not self.weight_cached:
+            plan.append(self._weight_cast(W))
+        plan.append(("gemm", lambda: B.gemm_fprop(self.Xq, self.Wq, b, B.EPI_BIAS_GELU, self.acc_mode, out=self.Y,
+                                                  aux=self.Z)))
+        return plan
 
     def _backward_plan(self, X, dY):
         if self.with_input_grad:
@@ -126,8 +142,10 @@ class LinearTrainStep:
     def launches(self, X, W, b, dY):
         return self._forward_plan(X, W, b) + self._backward_plan(X, dY)
 
-    # 4 casts + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
-    KERNELS_PER_STEP = 8
+    # 4 casts (3 with a cached weight) + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
+    @property
+    def KERNELS_PER_STEP(self):
+        return 7 if self.weight_cached else 8
 
 
 class MxLinearTrainStep(LinearTrainStep):
@@ -172,6 +190,9 @@ class MxLinearTrainStep(LinearTrainStep):
 
     def input_grad(self, W):
         raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+
+    def cache_weight(self, W):
+        raise NotImplementedError("weight caching is built for the 1x128 recipe")
 
     # 5 casts + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
     KERNELS_PER_STEP = 9
@@ -237,6 +258,9 @@ class TensorLinearTrainStep(LinearTrainStep):
 
     def input_grad(self, W):
         raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+
+    def cache_weight(self, W):
+        raise NotImplementedError("weight caching is built for the 1x128 recipe")
 
     # 4 casts + 3 GEMMs + bias-gradient finalize + 1 history update (delayed)
     @property

@@ -72,3 +72,26 @@ def test_train_step_with_two_way_casts_is_bit_identical(fp8):
     torch.cuda.synchronize()
     for a, c in zip(*outs):
         assert torch.equal(a, c)
+
+
+def test_cached_weight_steps_are_bit_identical(fp8):
+    # two micro-batch steps with W cast once up front equal two steps that
+    # cast W each time (every output, the accumulated dW and dX)
+    from fp8_linear_layer_gb300.linear import LinearTrainStep
+    m, k, n = 256, 384, 512
+    W = workloads.normal_bf16((n, k), 74, "w", std=0.02).cuda()
+    b = workloads.normal_bf16((n,), 74, "b", std=0.02).cuda()
+    batches = [(workloads.normal_bf16((m, k), 75 + i, "x").cuda(),
+                workloads.normal_bf16((m, k), 75 + i, "dy", std=1e-2).cuda()) for i in range(2)]
+    outs = []
+    for cached in (False, True):
+        st = LinearTrainStep(m, k, n, input_grad=True)
+        if cached:
+            st.cache_weight(W)
+            assert st.KERNELS_PER_STEP == 7
+        for X, dY in batches:
+            st.step(X, W, b, dY)
+        outs.append([t.clone() for t in (st.Y, st.Z, st.dZ, st.db, st.dW, st.input_grad(W))])
+    torch.cuda.synchronize()
+    for a, c in zip(*outs):
+        assert torch.equal(a, c)
