@@ -624,6 +624,9 @@ int fp8_tensor_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t 
         return FP8LL_ERR_INVALID_ARG;
     if (amax_out && ((reinterpret_cast<uintptr_t>(amax_out) & 3u) != 0 || amax_out == amax_in))
         return FP8LL_ERR_INVALID_ARG;
+    // the kernels read *amax_in while one thread writes *scale
+    if (static_cast<const void*>(scale) == static_cast<const void*>(amax_in) || scale == amax_out)
+        return FP8LL_ERR_INVALID_ARG;
     if (rows > (1LL << 31) - 1 || cols > (1LL << 31) - 1 || ldx < cols || ldx % 8 != 0) return FP8LL_ERR_INVALID_ARG;
     if (q_rows && (!aligned16(q_rows) || cols % 16 != 0)) return FP8LL_ERR_INVALID_ARG;
     if (q_cols && (!aligned16(q_cols) || rows % 128 != 0 || cols % 8 != 0 || rows / 128 > 65535))

@@ -305,8 +305,9 @@ int fp8_tensor_amax(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx,
  *   q_rows [rows][cols] (cols % 16 == 0), q_cols the transposed codes
  *   [cols][rows] (rows % 128 == 0, rows / 128 <= 65535, cols % 8 == 0); both
  *   together need cols % 128 == 0 and read x once.
- * *scale receives the dequantization scale.  amax_out (may be NULL, must not
- * be amax_in): receives max|x| of this x, for the history of the next step.
+ * *scale receives the dequantization scale (a word of its own: not amax_in or
+ * amax_out).  amax_out (may be NULL, must not be amax_in): receives max|x| of
+ * this x, for the history of the next step.
  * x as in fp8_tensor_amax.  rows == 0 or cols == 0 is a no-op. */
 int fp8_tensor_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,
                         uint8_t* q_rows, uint8_t* q_cols, float* scale, float* amax_out, fp8ll_stream_t stream);

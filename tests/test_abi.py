@@ -98,18 +98,20 @@ def test_tensor_scaling_validation(L):
     import fp8_linear_layer_gb300 as f
     E = f.binding.ERR_INVALID_ARG
     vp = ctypes.c_void_p
-    fake, other = vp(0x10000), vp(0x20000)
+    fake, other, sc = vp(0x10000), vp(0x20000), vp(0x40000)
     # amax: misaligned result, cols % 8
     assert L.fp8_tensor_amax(fake, 4, 128, 128, vp(0x10002), None) == E
     assert L.fp8_tensor_amax(fake, 4, 100, 128, other, None) == E
     # cast: no output, amax_out aliasing amax_in, rows-layout cols % 16,
     # transposed rows % 128, both orientations with cols % 128
-    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, None, None, other, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, None, None, sc, None, None) == E
     assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, fake, None, fake, other, None) == E
-    assert L.fp8_tensor_quantize(fake, 128, 200, 200, 0, other, fake, None, other, None, None) == E
-    assert L.fp8_tensor_quantize(fake, 100, 256, 256, 0, other, None, fake, other, None, None) == E
-    assert L.fp8_tensor_quantize(fake, 128, 136, 136, 0, other, fake, fake, other, None, None) == E
-    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 3, other, fake, None, other, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, fake, None, other, None, None) == E  # scale = amax_in
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 0, other, fake, None, vp(0x30000), vp(0x30000), None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 200, 200, 0, other, fake, None, sc, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 100, 256, 256, 0, other, None, fake, sc, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 136, 136, 0, other, fake, fake, sc, None, None) == E
+    assert L.fp8_tensor_quantize(fake, 128, 256, 256, 3, other, fake, None, sc, None, None) == E
     assert L.fp8_tensor_quantize(None, 0, 256, 256, 0, None, None, None, None, None, None) == 0  # empty
     # history: empty history
     assert L.fp8_amax_history_update(fake, 1, 0, other, other, None) == E
