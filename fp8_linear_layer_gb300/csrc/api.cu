@@ -333,7 +333,8 @@ int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     if (!valid_operand(A, M, K) || !valid_operand(B, N, K)) return FP8LL_ERR_INVALID_ARG;
     if (!out_bf16 || !aligned16(out_bf16)) return FP8LL_ERR_INVALID_ARG;
     if (epi != FP8LL_EPI_NONE && (!bias_bf16 || !aligned16(bias_bf16))) return FP8LL_ERR_INVALID_ARG;
-    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && (!aligned16(aux_bf16) || aux_bf16 == out_bf16))
+        return FP8LL_ERR_INVALID_ARG;
     DeviceInfo* dev = nullptr;
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
@@ -542,7 +543,8 @@ int fp8_mx_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
     if (epi != FP8LL_EPI_NONE && epi != FP8LL_EPI_BIAS && epi != FP8LL_EPI_BIAS_GELU) return FP8LL_ERR_INVALID_ARG;
     if (!out_bf16 || !aligned16(out_bf16)) return FP8LL_ERR_INVALID_ARG;
     if (epi != FP8LL_EPI_NONE && (!bias_bf16 || !aligned16(bias_bf16))) return FP8LL_ERR_INVALID_ARG;
-    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && (!aligned16(aux_bf16) || aux_bf16 == out_bf16))
+        return FP8LL_ERR_INVALID_ARG;
     TensorMaps maps;
     GemmParams p;
     DeviceInfo* dev = nullptr;
@@ -660,7 +662,8 @@ int fp8_tensor_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_op
     if (epi != FP8LL_EPI_NONE && epi != FP8LL_EPI_BIAS && epi != FP8LL_EPI_BIAS_GELU) return FP8LL_ERR_INVALID_ARG;
     if (!out_bf16 || !aligned16(out_bf16)) return FP8LL_ERR_INVALID_ARG;
     if (epi != FP8LL_EPI_NONE && (!bias_bf16 || !aligned16(bias_bf16))) return FP8LL_ERR_INVALID_ARG;
-    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (epi == FP8LL_EPI_BIAS_GELU && aux_bf16 && (!aligned16(aux_bf16) || aux_bf16 == out_bf16))
+        return FP8LL_ERR_INVALID_ARG;
     TensorMaps maps;
     GemmParams p;
     DeviceInfo* dev = nullptr;

@@ -156,8 +156,9 @@ int fp8_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, fp8ll_stream_t 
  *   A: M x K operand (X), B: N x K operand (W); K % 128 == 0, K >= 128.
  *   epi: FP8LL_EPI_NONE, _BIAS or _BIAS_GELU.  bias_bf16: [N] (required for
  *   BIAS / BIAS_GELU, ignored for NONE).  out_bf16: [M][N] contiguous.
- *   aux_bf16: [M][N] receives Z = C + bias for BIAS_GELU (may be NULL), unused
- *   otherwise.  acc_mode: FP8LL_ACC_FULL or _FAST.  M, N >= 1, any value. */
+ *   aux_bf16: [M][N] receives Z = C + bias for BIAS_GELU (may be NULL; not the
+ *   out_bf16 buffer), unused otherwise.  acc_mode: FP8LL_ACC_FULL or _FAST.
+ *   M, N >= 1, any value. */
 int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
                    const void* bias_bf16, int epi, int acc_mode, void* out_bf16, void* aux_bf16,
                    fp8ll_stream_t stream);

@@ -84,6 +84,7 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.fp8_gemm_fprop(8, 8, 256, ob, ob, fake, 3, 0, fake, fake, None) == E   # dgrad epilogue
     assert L.fp8_gemm_fprop(8, 8, 256, ob, ob, fake, 2, 5, fake, fake, None) == E   # bad acc mode
     assert L.fp8_gemm_fprop(0, 8, 256, ob, ob, fake, 2, 0, fake, fake, None) == E   # M = 0
+    assert L.fp8_gemm_fprop(8, 8, 256, ob, ob, fake, 2, 0, fake, fake, None) == E   # Y and Z share a buffer
     assert L.fp8_gemm_dgrad(8, 8, 256, ob, ob, fake, 4, 0, fake, fake, fake, 4, None) == f.binding.ERR_WORKSPACE
     assert L.fp8_gemm_dgrad(8, 8, 256, ob, ob, None, 3, 0, fake, None, None, 0, None) == E  # aux missing
     ks = (ctypes.c_int64 * 2)(128, 100)
