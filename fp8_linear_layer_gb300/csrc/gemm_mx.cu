@@ -10,9 +10,10 @@
 //               block's scale atoms (512 B for A, 1 KB for B, untiled bulk
 //               copies) into one 4-stage ring.
 //   warp 1      TMEM owner and MMA issuer: per K block, three tcgen05.cp copy
-//               the scale atoms into a tensor-memory scale slot (4 slots,
-//               12 columns each: lane l, column c = the four 32-element scales
-//               of row l + 32c, B's rows 128..255 four columns further), then
+//               the scale atoms into a tensor-memory scale slot (4 slots of
+//               16 columns, 12 used: lane l, column c = the four 32-element
+//               scales of row l + 32c, B's rows 128..255 four columns
+//               further), then
 //               four block-scaled MMAs (M=128, N=256, K=32, scale id = the
 //               32-element group) accumulate into one 256-column accumulator.
 //   warps 4-11  epilogue: once per tile, the accumulator is read (16x256b
