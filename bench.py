@@ -80,6 +80,8 @@ def parse_args():
                          "tensor: one scale per tensor (delayed scaling), scaled once after the K loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--e2e-read-dw", action="store_true",
+                    help="end-to-end leg: read the fp32 dW back every step as well (235 MB at the default size)")
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
@@ -267,12 +269,15 @@ def run_reference(args):
 
 def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
     """The same step through the public API with host buffers: each step copies
-    its X, W, b, dY from pinned host memory and reads its dW and db back, all
-    inside the timed region.  The copies run on their own streams so that they
-    overlap the neighbouring steps' kernels: inputs alternate between two device
-    buffer sets (step i+1's inputs arrive while step i computes), and each
-    step's dW is copied to a device snapshot that is read back while the next
-    step computes (the next snapshot waits for that read-back)."""
+    its X, W, b, dY from pinned host memory and reads its result back, all
+    inside the timed region.  The result read back is the bias gradient db (the
+    step's small output; dW stays on the device for the optimizer); with
+    --e2e-read-dw the 235 MB fp32 dW is read back every step as well.  The
+    copies run on their own streams so that they overlap the neighbouring
+    steps' kernels: inputs alternate between two device buffer sets (step i+1's
+    inputs arrive while step i computes), and a dW read back goes through a
+    device snapshot that is copied to the host while the next step computes
+    (the next snapshot waits for that read-back)."""
     import torch
     hX, hW, hb, hdY = host
     flops_step = step.gemm_flops
@@ -284,9 +289,10 @@ def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
     set_free = [torch.cuda.Event() for _ in range(2)]
     out_done = torch.cuda.Event()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h_dW = torch.empty(step.dW.shape, dtype=torch.float32).pin_memory()
+    read_dw = args.e2e_read_dw
+    h_dW = torch.empty(step.dW.shape, dtype=torch.float32).pin_memory() if read_dw else None
     h_db = torch.empty(step.db.shape, dtype=torch.float32).pin_memory()
-    dW_snap = torch.empty_like(step.dW)
+    dW_snap = torch.empty_like(step.dW) if read_dw else None
     e2e_steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     barrier()
@@ -310,25 +316,28 @@ def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
         # (once the previous snapshot has been read back) and from there to the
         # host on the copy stream
         h_db.copy_(step.db, non_blocking=True)
-        if i >= 1:
-            stream.wait_event(out_done)
-        dW_snap.copy_(step.dW)
-        step_done = torch.cuda.Event()
-        step_done.record(stream)
-        with torch.cuda.stream(copy_out):
-            copy_out.wait_event(step_done)
-            h_dW.copy_(dW_snap, non_blocking=True)
-            out_done.record(copy_out)
-    stream.wait_event(out_done)
+        if read_dw:
+            if i >= 1:
+                stream.wait_event(out_done)
+            dW_snap.copy_(step.dW)
+            step_done = torch.cuda.Event()
+            step_done.record(stream)
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(step_done)
+                h_dW.copy_(dW_snap, non_blocking=True)
+                out_done.record(copy_out)
+    if read_dw:
+        stream.wait_event(out_done)
     ev1.record(stream)
     ev1.synchronize()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hb, hdY))
-    d2h = h_dW.numel() * 4 + h_db.numel() * 4
+    d2h = (h_dW.numel() * 4 if read_dw else 0) + h_db.numel() * 4
     e2e_value = tflops(world, flops_step, e2e_steps, e2e_ms)
     return {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": e2e_steps, "overlap": "copies on separate streams, two input buffer sets, dW read back "
-                                           "from a device snapshot"}
+            "steps": e2e_steps, "result_read_back": "db and dW" if read_dw else "db (dW stays on the device)",
+            "overlap": "copies on separate streams, two input buffer sets"
+                       + (", dW read back from a device snapshot" if read_dw else "")}
 
 
 def run_ours(args):
