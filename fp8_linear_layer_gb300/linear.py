@@ -189,7 +189,18 @@ class MxLinearTrainStep(LinearTrainStep):
         ]
 
     def input_grad(self, W):
-        raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+        """dX = dZ W (m x k, bf16) on MXFP8 operands: dZ cast by rows (e5m2),
+        W down its columns (e4m3), the block-scaled GEMM without an epilogue.
+        Needs ``backward`` first."""
+        if not hasattr(self, "dX"):
+            dev = self.dZ.device
+            self.dZq = B.empty_mx(self.m, self.n, B.E5M2, dev)
+            self.WTq = B.empty_mx(self.k, self.n, B.E4M3, dev)
+            self.dX = torch.empty((self.m, self.k), dtype=torch.bfloat16, device=dev)
+        B.mx_quantize(self.dZ, B.E5M2, out=self.dZq)
+        B.mx_quantize(W, B.E4M3, transpose=True, out=self.WTq)
+        B.mx_gemm_fprop(self.dZq, self.WTq, None, B.EPI_NONE, out=self.dX)
+        return self.dX
 
     def cache_weight(self, W):
         raise NotImplementedError("weight caching is built for the 1x128 recipe")
@@ -257,7 +268,20 @@ class TensorLinearTrainStep(LinearTrainStep):
         return plan
 
     def input_grad(self, W):
-        raise NotImplementedError("the input gradient is built for the 1x128 recipe")
+        """dX = dZ W (m x k, bf16) on per-tensor scaled operands: dZ cast by
+        rows (e5m2) and W down its columns (e4m3), each with its own amax
+        (current scaling, an amax pass first), then the GEMM without an
+        epilogue.  Needs ``backward`` first."""
+        if not hasattr(self, "dX"):
+            dev = self.dZ.device
+            self.dZq = B.empty_tensor_scaled(self.m, self.n, B.E5M2, dev)
+            self.WTq = B.empty_tensor_scaled(self.k, self.n, B.E4M3, dev)
+            self.dX = torch.empty((self.m, self.k), dtype=torch.bfloat16, device=dev)
+            self.amax_ig = torch.zeros((2, 1), dtype=torch.float32, device=dev)
+        B.tensor_quantize(self.dZ, B.E5M2, B.tensor_amax(self.dZ, out=self.amax_ig[0]), out=self.dZq)
+        B.tensor_quantize(W, B.E4M3, B.tensor_amax(W, out=self.amax_ig[1]), rows=False, cols=True, out_t=self.WTq)
+        B.tensor_gemm_fprop(self.dZq, self.WTq, None, B.EPI_NONE, out=self.dX)
+        return self.dX
 
     def cache_weight(self, W):
         raise NotImplementedError("weight caching is built for the 1x128 recipe")

@@ -95,3 +95,42 @@ def test_cached_weight_steps_are_bit_identical(fp8):
     torch.cuda.synchronize()
     for a, c in zip(*outs):
         assert torch.equal(a, c)
+
+
+def test_mx_step_input_grad_vs_oracle(fp8):
+    from fp8_linear_layer_gb300.linear import MxLinearTrainStep
+    m, k, n = 256, 384, 512
+    X = workloads.normal_bf16((m, k), 76, "x").cuda()
+    W = workloads.normal_bf16((n, k), 76, "w", std=0.02)
+    b = workloads.normal_bf16((n,), 76, "b", std=0.02).cuda()
+    dY = workloads.normal_bf16((m, k), 76, "dy", std=1e-2).cuda()
+    st = MxLinearTrainStep(m, k, n)
+    st.step(X, W.cuda(), b, dY)
+    dX = st.input_grad(W.cuda())
+    torch.cuda.synchronize()
+    qa, ea = oracle.mx_quantize(workloads.bits(st.dZ.cpu()), E5M2)
+    qb, eb = oracle.mx_quantize(workloads.bits(W), E4M3, transpose=True)
+    assert np.array_equal(st.dZq.q.cpu().numpy(), qa) and np.array_equal(st.WTq.q.cpu().numpy(), qb)
+    acc, S = oracle.mx_gemm(qa, ea, E5M2, qb, eb, E4M3)
+    got = bf16_to_f64(dX)
+    assert_within(got, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(got), np.abs(acc))), "dX")
+
+
+def test_per_tensor_step_input_grad_vs_oracle(fp8):
+    from fp8_linear_layer_gb300.linear import TensorLinearTrainStep
+    m, k, n = 256, 384, 512
+    X = workloads.normal_bf16((m, k), 77, "x").cuda()
+    W = workloads.normal_bf16((n, k), 77, "w", std=0.02)
+    b = workloads.normal_bf16((n,), 77, "b", std=0.02).cuda()
+    dY = workloads.normal_bf16((m, k), 77, "dy", std=1e-2).cuda()
+    st = TensorLinearTrainStep(m, k, n)
+    st.step(X, W.cuda(), b, dY)
+    dX = st.input_grad(W.cuda())
+    torch.cuda.synchronize()
+    dz = st.dZ.cpu()
+    qa, sa, _ = oracle.tensor_quantize(workloads.bits(dz), E5M2, float(dz.abs().max()))
+    qb, sb, _ = oracle.tensor_quantize(workloads.bits(W), E4M3, float(W.abs().max()), transpose=True)
+    assert np.array_equal(st.dZq.q.cpu().numpy(), qa) and np.array_equal(st.WTq.q.cpu().numpy(), qb)
+    acc, S = oracle.tensor_gemm(qa, sa, E5M2, qb, sb, E4M3)
+    got = bf16_to_f64(dX)
+    assert_within(got, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(got), np.abs(acc))), "dX")
