@@ -80,6 +80,8 @@ def parse_args():
                          "tensor: one scale per tensor (delayed scaling), scaled once after the K loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--e2e-copy-weights", action="store_true",
+                    help="end-to-end leg: copy W and b from the host every step as well")
     ap.add_argument("--e2e-read-dw", action="store_true",
                     help="end-to-end leg: read the fp32 dW back every step as well (235 MB at the default size)")
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
@@ -269,10 +271,12 @@ def run_reference(args):
 
 def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
     """The same step through the public API with host buffers: each step copies
-    its X, W, b, dY from pinned host memory and reads its result back, all
-    inside the timed region.  The result read back is the bias gradient db (the
-    step's small output; dW stays on the device for the optimizer); with
-    --e2e-read-dw the 235 MB fp32 dW is read back every step as well.  The
+    its batch (X, dY) from pinned host memory and reads its result back, all
+    inside the timed region.  The layer's parameters W and b stay on the device
+    as in training, where the optimizer updates them there (--e2e-copy-weights
+    copies them every step as well); the result read back is the bias gradient
+    db (dW stays on the device for the optimizer; --e2e-read-dw reads the
+    235 MB fp32 dW back every step as well).  The
     copies run on their own streams so that they overlap the neighbouring
     steps' kernels: inputs alternate between two device buffer sets (step i+1's
     inputs arrive while step i computes), and a dW read back goes through a
@@ -282,6 +286,11 @@ def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
     hX, hW, hb, hdY = host
     flops_step = step.gemm_flops
     sets = [tuple(dev_in), tuple(torch.empty_like(t) for t in dev_in)]
+    copy_w = args.e2e_copy_weights
+    per_step = (0, 1, 2, 3) if copy_w else (0, 3)  # which of X, W, b, dY cross the link each step
+    for t in range(4):
+        if t not in per_step:
+            sets[1][t].copy_(sets[0][t])  # resident parameters in both buffer sets
     plans = [step.launches(*s) for s in sets]
     copy_in = torch.cuda.Stream(device=dev)
     copy_out = torch.cuda.Stream(device=dev)
@@ -304,8 +313,8 @@ def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
         with torch.cuda.stream(copy_in):
             if i >= 2:
                 copy_in.wait_event(set_free[s])
-            for dst, src in zip(sets[s], (hX, hW, hb, hdY)):
-                dst.copy_(src, non_blocking=True)
+            for t in per_step:
+                sets[s][t].copy_((hX, hW, hb, hdY)[t], non_blocking=True)
             in_ready[s].record(copy_in)
         stream.wait_event(in_ready[s])
         for _, fn in plans[s]:
@@ -331,11 +340,12 @@ def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
     ev1.record(stream)
     ev1.synchronize()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hb, hdY))
+    h2d = sum((hX, hW, hb, hdY)[t].numel() * (hX, hW, hb, hdY)[t].element_size() for t in per_step)
     d2h = (h_dW.numel() * 4 if read_dw else 0) + h_db.numel() * 4
     e2e_value = tflops(world, flops_step, e2e_steps, e2e_ms)
     return {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": e2e_steps, "result_read_back": "db and dW" if read_dw else "db (dW stays on the device)",
+            "steps": e2e_steps, "copied_in": "X, W, b, dY" if copy_w else "X, dY (W, b resident)",
+            "result_read_back": "db and dW" if read_dw else "db (dW stays on the device)",
             "overlap": "copies on separate streams, two input buffer sets"
                        + (", dW read back from a device snapshot" if read_dw else "")}
 
