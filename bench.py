@@ -80,6 +80,9 @@ def parse_args():
                          "tensor: one scale per tensor (delayed scaling), scaled once after the K loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="name every launch of the step with an NVTX range (for an external profiler's "
+                         "timeline; adds host work, so not for timed runs)")
     ap.add_argument("--e2e-copy-weights", action="store_true",
                     help="end-to-end leg: copy W and b from the host every step as well")
     ap.add_argument("--e2e-read-dw", action="store_true",
@@ -269,6 +272,19 @@ def run_reference(args):
     return 0
 
 
+def nvtx_named(name, fn):
+    """fn wrapped in an NVTX range of that name."""
+    import torch
+
+    def wrapped():
+        torch.cuda.nvtx.range_push(name)
+        try:
+            fn()
+        finally:
+            torch.cuda.nvtx.range_pop()
+    return wrapped
+
+
 def run_e2e(args, step, host, dev_in, stream, barrier, world, dev):
     """The same step through the public API with host buffers: each step copies
     its batch (X, dY) from pinned host memory and reads its result back, all
@@ -379,6 +395,8 @@ def run_ours(args):
     else:
         step = LinearTrainStep(m, k, n, dev, acc_mode)
     launches = step.launches(X, W, b, dY)
+    if args.nvtx:
+        launches = [(kind, nvtx_named("%d:%s" % (j, kind), fn)) for j, (kind, fn) in enumerate(launches)]
     stream = torch.cuda.current_stream()
 
     for _ in range(max(3, args.warmup)):
