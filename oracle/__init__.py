@@ -72,6 +72,7 @@ def _load():
         lib.oracle_gelu_array.argtypes = [vp, vp, i64]
         lib.oracle_dgelu_array.argtypes = [vp, vp, i64]
         lib.oracle_colsum.argtypes = [vp, i64, i64, vp]
+        lib.oracle_operand_rowsum.argtypes = [i32, vp, i64, vp, i64, i64, i64, vp, vp]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -297,6 +298,24 @@ def colsum(dz) -> np.ndarray:
     out = np.empty(N, dtype=np.float64)
     _load().oracle_colsum(_p(dz), M, N, _p(out))
     return out
+
+
+def operand_rowsum(q, scale, fmt: int, want_abs=True):
+    """Bias gradient reduced from the weight-gradient GEMM's fp8 operand
+    (BGRADB on "Replaced cublasLt calls with rocblas gemm + 6 manually crafted
+    epilogues": db computed with dW by reducing its gradient operand):
+    out[r] = sum_k scale[k // 128, r] * dec(q[r, k]), binary64.  `q` is
+    [rows][K] codes, `scale` [K/128][>= rows] fp32.  Returns (out, S) with S
+    the magnitude sums (None unless want_abs)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    rows, K = q.shape
+    assert K % 128 == 0 and scale.shape[0] == K // 128 and scale.shape[1] >= rows
+    out = np.empty(rows, dtype=np.float64)
+    S = np.empty(rows, dtype=np.float64) if want_abs else None
+    _load().oracle_operand_rowsum(fmt, _p(q), K, _p(scale), scale.shape[1], rows, K, _p(out),
+                                  _p(S) if want_abs else None)
+    return out, S
 
 
 def fprop_epilogue(acc, bias_bits=None, cols=None, gelu_on=True):

@@ -505,6 +505,30 @@ void oracle_colsum(const double* dz, int64_t M, int64_t N, double* out)
     }
 }
 
+/* BGRADB ([P1] backward): db is taken together with dW by reducing the
+ * gradient operand of the weight-gradient GEMM over that GEMM's k (the
+ * tokens).  With the operand cast to fp8 by 1x128 blocks, this is
+ *   db[r] = sum_k scale[k/128][r] * dec(q[r][k]),
+ * summed element by element in binary64.  S[r] = sum_k |scale * dec| (the
+ * magnitude sum the error bound is taken against), or skipped when S is NULL. */
+void oracle_operand_rowsum(int fmt, const uint8_t* q, int64_t ldq, const float* scale, int64_t scale_ld,
+                           int64_t rows, int64_t K, double* out, double* S)
+{
+    build_tables();
+    const double* t = g_table[fmt ? 1 : 0];
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double total = 0.0, total_abs = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double v = (double)scale[(k / 128) * scale_ld + r] * t[q[r * ldq + k]];
+            total += v;
+            total_abs += fabs(v);
+        }
+        out[r] = total;
+        if (S) S[r] = total_abs;
+    }
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

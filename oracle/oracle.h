@@ -75,6 +75,12 @@ void   oracle_dgelu_array(const double* z, double* y, int64_t n);
 /* column sums over all rows of a dense [M][N] double matrix: bgrad[j] = sum_i dz[i][j] */
 void oracle_colsum(const double* dz, int64_t M, int64_t N, double* out);
 
+/* bias gradient reduced from the weight-gradient GEMM's 1x128-scaled fp8
+ * operand: out[r] = sum_k scale[k/128][r] dec(q[r][k]); S (or NULL) the sum of
+ * the magnitudes */
+void oracle_operand_rowsum(int fmt, const uint8_t* q, int64_t ldq, const float* scale, int64_t scale_ld,
+                           int64_t rows, int64_t K, double* out, double* S);
+
 int oracle_num_threads(void);
 
 #ifdef __cplusplus

@@ -97,6 +97,26 @@ def run_pins_on_mutant(tmp_path, old, new, name, pin_tests):
     assert r.returncode != 0, "pins did not catch: %s\n%s" % (name, r.stdout[-2000:])
 
 
+# bias gradient reduced from the fp8 operand: checked against its own pin file only
+BGRADB_MUTANTS = {
+    "operand row sum reads the scale of another row": (
+        "const double v = (double)scale[(k / 128) * scale_ld + r] * t[q[r * ldq + k]];",
+        "const double v = (double)scale[(k / 128) * scale_ld + r / 2] * t[q[r * ldq + k]];"),
+    "operand row sum uses the first block's scale": (
+        "const double v = (double)scale[(k / 128) * scale_ld + r] * t[q[r * ldq + k]];",
+        "const double v = (double)scale[r] * t[q[r * ldq + k]];"),
+    "operand row sum decodes with the wrong format": (
+        "    const double* t = g_table[fmt ? 1 : 0];\n#pragma omp parallel for schedule(static)\n    for (int64_t r = 0;",
+        "    const double* t = g_table[0];\n#pragma omp parallel for schedule(static)\n    for (int64_t r = 0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BGRADB_MUTANTS))
+def test_bgradb_pins_catch_mutant(name, tmp_path):
+    old, new = BGRADB_MUTANTS[name]
+    run_pins_on_mutant(tmp_path, old, new, name, ["tests/test_oracle_bgrad_operand.py"])
+
+
 @pytest.mark.parametrize("name", sorted(TENSOR_MUTANTS))
 def test_tensor_pins_catch_mutant(name, tmp_path):
     old, new = TENSOR_MUTANTS[name]
