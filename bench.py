@@ -78,6 +78,9 @@ def parse_args():
                     help="block128: one fp32 scale per 128 elements, promoted in software (the configured "
                          "workload); mx: MXFP8, one power-of-two scale per 32 elements applied by the tensor core; "
                          "tensor: one scale per tensor (delayed scaling), scaled once after the K loop")
+    ap.add_argument("--bias-grad", choices=["dgrad", "operand"], default="dgrad",
+                    help="1x128 step: db from the data-gradient GEMM's epilogue (default) or reduced from the "
+                         "weight-gradient GEMM's fp8 operand dZ^T")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--nvtx", action="store_true",
@@ -393,7 +396,7 @@ def run_ours(args):
         from fp8_linear_layer_gb300.linear import TensorLinearTrainStep
         step = TensorLinearTrainStep(m, k, n, dev)
     else:
-        step = LinearTrainStep(m, k, n, dev, acc_mode)
+        step = LinearTrainStep(m, k, n, dev, acc_mode, bias_grad=args.bias_grad)
     launches = step.launches(X, W, b, dY)
     if args.nvtx:
         launches = [(kind, nvtx_named("%d:%s" % (j, kind), fn)) for j, (kind, fn) in enumerate(launches)]
@@ -464,9 +467,11 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8(e4m3/e5m2) x fp8 -> fp32 accumulate", "data": "synthetic",
             "config": {"workload": (WORKLOAD if default_size else "linear_train_step_m%d_k%d_n%d_bias_gelu" % (m, k, n))
-                       + {"block128": "", "mx": "_mxfp8", "tensor": "_per_tensor_delayed"}[args.recipe],
+                       + {"block128": "", "mx": "_mxfp8", "tensor": "_per_tensor_delayed"}[args.recipe]
+                       + ("_bgrad_from_operand" if args.recipe == "block128" and args.bias_grad == "operand" else ""),
                        "m_tokens": m, "k_in": k, "n_out": n,
                        "acc_mode": args.acc if args.recipe == "block128" else None, "recipe": args.recipe,
+                       "bias_grad": args.bias_grad if args.recipe == "block128" else "dgrad",
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
@@ -475,7 +480,8 @@ def run_ours(args):
                          + " (fprop, dgrad, wgrad launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),
-                         "traffic": measured_traffic() if default_size and args.recipe == "block128" else None,
+                         "traffic": measured_traffic()
+                         if default_size and args.recipe == "block128" and args.bias_grad == "dgrad" else None,
                          "traffic_unit": "bytes",
                          "avg_gemm_ms": avg_gemm_ms},
             "e2e": e2e,
@@ -581,6 +587,25 @@ def run_kernel_study(args):
         e.synchronize()
         return s.elapsed_time(e) / reps
 
+    def graph_timed(fn):
+        # a kernel shorter than the host's per-call overhead: `reps` launches
+        # replayed from one CUDA graph, so the device time is what is measured
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.replay()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps
+
     out = {"study": "kernels", "reps": reps, "gemm_tflops": {}, "cast_gbs": {}}
     x = workloads.normal_bf16((m, k), SEED, "X").cuda()
     w = workloads.normal_bf16((n, k), SEED, "W", std=0.02).cuda()
@@ -594,7 +619,13 @@ def run_kernel_study(args):
         lambda: fp8.gemm_fprop(X, W, bias, fp8.EPI_BIAS_GELU, out=Y, aux=Z))
     out["gemm_tflops"]["dgrad_dgelu_bgrad_m%d_n%d_k%d" % (m, n, k)] = f / timed(
         lambda: fp8.gemm_dgrad(DY, W, Z, fp8.EPI_DGELU_BGRAD, out=dZ))
+    out["gemm_tflops"]["dgrad_dgelu_m%d_n%d_k%d" % (m, n, k)] = f / timed(
+        lambda: fp8.gemm_dgrad(DY, W, Z, fp8.EPI_DGELU, out=dZ))
     DZT, XT = fp8.quantize(dZ, fp8.E5M2, transpose=True), fp8.quantize(x, fp8.E4M3, transpose=True)
+    # the bias gradient reduced from dZ^T's codes: K + 4 K/128 bytes read, 4 written per row
+    db = torch.empty((n,), dtype=torch.float32, device="cuda")
+    out["reduce_gbs"] = {"bgrad_from_operand_e5m2_%dx%d" % (n, m): n * (m + 4.0 * m / 128 + 4) / 1e6 / graph_timed(
+        lambda: fp8.bgrad_from_operand(DZT, out=db))}
     dW = torch.zeros((n, k), device="cuda")
     out["gemm_tflops"]["wgrad_accumulate_m%d_n%d_k%d" % (n, k, m)] = f / timed(lambda: fp8.gemm_wgrad(DZT, XT, dW))
     for (M, N, K) in ((16384, 7168, 8192), (8192, 8192, 16384)):

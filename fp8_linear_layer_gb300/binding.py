@@ -26,7 +26,8 @@ EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", 
            "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
            "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
            "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize",
-           "fp8_amax_history_update", "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad")
+           "fp8_amax_history_update", "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
+           "fp8_bgrad_from_operand")
 
 
 class Fp8Error(RuntimeError):
@@ -93,11 +94,13 @@ def lib():
         L.fp8_tensor_gemm_fprop.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp]
         L.fp8_tensor_gemm_dgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp, sz, vp]
         L.fp8_tensor_gemm_wgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp]
+        L.fp8_bgrad_from_operand.argtypes = [i64, i64, op, vp, i32, vp]
         for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
                      "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
                      "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize", "fp8_amax_history_update",
                      "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
-                     "fp8_grouped_wgrad", "fp8_get_device_status", "fp8_debug_starve_next_gemm"):
+                     "fp8_grouped_wgrad", "fp8_bgrad_from_operand", "fp8_get_device_status",
+                     "fp8_debug_starve_next_gemm"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -252,6 +255,18 @@ def grouped_wgrad(A: Fp8Tensor, B: Fp8Tensor, k_sizes: Sequence[int], out: torch
     oa, ob = A.operand(), B.operand()
     _check(lib().fp8_grouped_wgrad(G, M, N, ks, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
                                    int(bool(accumulate)), int(acc), _stream()), "fp8_grouped_wgrad")
+    return out
+
+
+def bgrad_from_operand(A: Fp8Tensor, out: Optional[torch.Tensor] = None, accumulate: bool = False) -> torch.Tensor:
+    """fp32 db [rows] (+)= the row sums of the dequantized operand A: the bias
+    gradient reduced from the weight-gradient GEMM's gradient operand dZ^T."""
+    if out is None:
+        out = torch.empty(A.rows, dtype=torch.float32, device=A.q.device)
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (A.rows,)
+    oa = A.operand()
+    _check(lib().fp8_bgrad_from_operand(A.rows, A.k, ctypes.byref(oa), _ptr(out), int(bool(accumulate)), _stream()),
+           "fp8_bgrad_from_operand")
     return out
 
 

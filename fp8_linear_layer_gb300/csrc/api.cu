@@ -473,6 +473,30 @@ int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     return fp8_grouped_wgrad(1, M, N, ks, A, B, out, accumulate, acc_mode, stream);
 }
 
+// true when [a, a + na) and [b, b + nb) share a byte
+static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+}
+
+int fp8_bgrad_from_operand(int64_t rows, int64_t K, const fp8ll_operand_t* A, float* db, int accumulate,
+                           fp8ll_stream_t stream) {
+    if (rows < 0 || K < 0 || K % 128 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (rows == 0) return FP8LL_OK;
+    if (!db || (reinterpret_cast<uintptr_t>(db) & 3u) != 0 || !valid_operand(A, rows, K)) return FP8LL_ERR_INVALID_ARG;
+    // the kernel reads codes and scales through the read-only path: db may overlap neither
+    const int64_t qbytes = (rows - 1) * A->ld_q + K;
+    const int64_t sbytes = K > 0 ? ((K / 128 - 1) * A->scale_ld + rows) * 4 : 0;
+    if (overlaps(db, rows * 4, A->q, qbytes) || overlaps(db, rows * 4, A->scale, sbytes)) return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_operand_rowsum(A->q, A->ld_q, A->scale, A->scale_ld, A->fmt, rows, K, db, accumulate ? 1 : 0,
+                                 reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
 int fp8_get_device_status(fp8ll_stream_t stream) {
     DeviceInfo* dev = nullptr;
     int rc = current_device(&dev);

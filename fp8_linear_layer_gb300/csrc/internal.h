@@ -20,6 +20,8 @@ int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
                            int num_sms);
 int launch_amax_history(float* hist, int64_t count, int64_t len, const float* amax_new, float* amax_use,
                         cudaStream_t stream);
+int launch_operand_rowsum(const uint8_t* q, int64_t ldq, const float* scale, int64_t sld, int fmt, int64_t rows,
+                          int64_t K, float* db, int accumulate, cudaStream_t stream, int num_sms);
 int64_t mx_sf_groups(int64_t rows);
 int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int transpose, uint8_t* q,
                        uint8_t* sf, cudaStream_t stream, int num_sms);

@@ -33,11 +33,19 @@ from . import binding as B
 
 class LinearTrainStep:
     def __init__(self, m: int, k: int, n: int, device="cuda", acc_mode: int = B.ACC_FULL,
-                 input_grad: bool = False):
+                 input_grad: bool = False, bias_grad: str = "dgrad"):
+        """``bias_grad`` picks where db comes from: "dgrad" sums the fp32 dZ in
+        the data-gradient GEMM's epilogue (before any fp8 rounding); "operand"
+        reduces the weight-gradient GEMM's fp8 operand dZ^T over the tokens
+        (the BGRADB form: db taken together with dW from the gradient operand,
+        "Replaced cublasLt calls with rocblas gemm + 6 manually crafted
+        epilogues"), after a data-gradient GEMM without the sums."""
         assert m % 128 == 0 and k % 128 == 0
         assert not input_grad or n % 128 == 0, "the two-way casts of W and dZ need n % 128 == 0"
+        assert bias_grad in ("dgrad", "operand")
         self.m, self.k, self.n = m, k, n
         self.acc_mode = acc_mode
+        self.bias_grad = bias_grad
         self.with_input_grad = input_grad
         self.weight_cached = False
         dev = torch.device(device)
@@ -100,13 +108,23 @@ class LinearTrainStep:
             cast_dz = ("quantize", lambda: B.quantize_dual(self.dZ, B.E5M2, out=self.dZq, out_t=self.dZTq))
         else:
             cast_dz = ("quantize", lambda: B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq))
-        return [
-            ("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq)),
-            ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode,
-                                          out=self.dZ, bgrad=self.db, workspace=self.ws)),
-            cast_dz,
-            ("gemm", lambda: B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True, acc=self.acc_mode)),
-        ]
+        plan = [("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq))]
+        if self.bias_grad == "operand":
+            plan += [
+                ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, self.acc_mode, out=self.dZ)),
+                cast_dz,
+                # right after the cast, while much of dZ^T is still in L2
+                ("reduce", lambda: B.bgrad_from_operand(self.dZTq, out=self.db)),
+            ]
+        else:
+            plan += [
+                ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, self.acc_mode,
+                                              out=self.dZ, bgrad=self.db, workspace=self.ws)),
+                cast_dz,
+            ]
+        plan.append(("gemm", lambda: B.gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True,
+                                                  acc=self.acc_mode)))
+        return plan
 
     def forward(self, X, W, b):
         for _, launch in self._forward_plan(X, W, b):
@@ -142,7 +160,8 @@ class LinearTrainStep:
     def launches(self, X, W, b, dY):
         return self._forward_plan(X, W, b) + self._backward_plan(X, dY)
 
-    # 4 casts (3 with a cached weight) + fprop GEMM + dgrad GEMM + bias-gradient finalize + wgrad GEMM
+    # 4 casts (3 with a cached weight) + fprop GEMM + dgrad GEMM + bias-gradient finalize (or the
+    # reduction of dZ^T's codes) + wgrad GEMM
     @property
     def KERNELS_PER_STEP(self):
         return 7 if self.weight_cached else 8

@@ -13,6 +13,7 @@
  *   fp8_gemm_dgrad      C = A B^T times gelu'(Z), optional bias-gradient sums
  *   fp8_gemm_wgrad      fp32 out (+)= A B^T
  *   fp8_grouped_wgrad   per-group fp32 out_g (+)= A_g B_g^T, groups along K
+ *   fp8_bgrad_from_operand  bias gradient as row sums of a 1x128-scaled operand
  *
  * Conventions shared by every entry point
  *   - One row-major "NT" convention: C[M][N] = A[M][K] . B[N][K]^T; both
@@ -221,6 +222,23 @@ int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
  *   1 <= G <= 256.  A.ld_q, B.ld_q >= sum of k_sizes. */
 int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const fp8ll_operand_t* A,
                       const fp8ll_operand_t* B, float* out, int accumulate, int acc_mode, fp8ll_stream_t stream);
+
+/* Bias gradient reduced from the weight-gradient GEMM's gradient operand
+ * (the BGRADB epilogue on "Replaced cublasLt calls with rocblas gemm + 6
+ * manually crafted epilogues": db is taken together with dW by reducing the
+ * gradient operand over that GEMM's k, the tokens).  For A the [rows][K]
+ * operand dZ^T (features x tokens, from the transposed cast of dZ):
+ *   db[r] (+)= sum_kb A.scale[kb][r] * sum_{k in block kb} dec(A.q[r][k])
+ *   db: fp32 [rows], 4-byte aligned; it may overlap neither A's codes nor its
+ *       scales (FP8LL_ERR_INVALID_ARG).
+ *   accumulate = 1: db[r] += the sum; 0: db[r] = the sum.
+ *   K % 128 == 0; K == 0 gives a sum of 0.  rows == 0 is a no-op.
+ * The sums run in fp32 in a fixed order: results are deterministic.  This is
+ * the alternative to the bias-gradient sums of fp8_gemm_dgrad's
+ * FP8LL_EPI_DGELU_BGRAD, which add up the fp32 dZ before any fp8 rounding;
+ * this one adds up the fp8 values the weight gradient consumes. */
+int fp8_bgrad_from_operand(int64_t rows, int64_t K, const fp8ll_operand_t* A, float* db, int accumulate,
+                           fp8ll_stream_t stream);
 
 /* ------------------------------------------------------------------ MXFP8
  * The MX block format, named among the fp8 recipes on "How can we use

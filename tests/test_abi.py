@@ -152,3 +152,21 @@ def test_mx_sizes_and_validation(L):
     assert L.fp8_mx_gemm_dgrad(128, 128, 256, ctypes.byref(op), ctypes.byref(op), None, 4, out, None, None, 0,
                                None) == E
 
+
+
+def test_bgrad_from_operand_validation(L):
+    import fp8_linear_layer_gb300 as f
+    E = f.binding.ERR_INVALID_ARG
+    vp = ctypes.c_void_p
+    q, s = 0x100000, 0x200000  # never dereferenced: validation fails first
+    op = f.binding.OperandStruct(q, s, 256, 8, f.E4M3, 0)
+    fn = L.fp8_bgrad_from_operand
+    assert fn(8, 200, ctypes.byref(op), vp(0x300000), 0, None) == E  # K % 128
+    assert fn(8, 256, ctypes.byref(op), vp(0x300002), 0, None) == E  # db misaligned
+    assert fn(8, 256, ctypes.byref(op), None, 0, None) == E
+    assert fn(9, 256, ctypes.byref(op), vp(0x300000), 0, None) == E  # scale_ld < rows
+    assert fn(8, 256, ctypes.byref(op), vp(q + 7 * 256 + 200), 0, None) == E  # db inside the codes
+    assert fn(8, 256, ctypes.byref(op), vp(s + 4 * 8 + 16), 0, None) == E  # db inside block 1's scales
+    assert fn(8, 256, ctypes.byref(op), vp(q - 28), 0, None) == E  # db's last element on the first code
+    assert fn(0, 256, ctypes.byref(op), None, 0, None) == f.binding.OK  # no rows: nothing to do
+    assert fn(-1, 256, ctypes.byref(op), vp(0x300000), 0, None) == E
