@@ -78,9 +78,9 @@ def parse_args():
                     help="block128: one fp32 scale per 128 elements, promoted in software (the configured "
                          "workload); mx: MXFP8, one power-of-two scale per 32 elements applied by the tensor core; "
                          "tensor: one scale per tensor (delayed scaling), scaled once after the K loop")
-    ap.add_argument("--bias-grad", choices=["dgrad", "operand"], default="dgrad",
-                    help="1x128 step: db from the data-gradient GEMM's epilogue (default) or reduced from the "
-                         "weight-gradient GEMM's fp8 operand dZ^T")
+    ap.add_argument("--bias-grad", choices=["cast", "dgrad", "operand"], default="cast",
+                    help="1x128 step: db from the transposed cast of dZ (default), from the data-gradient GEMM's "
+                         "epilogue, or reduced from the weight-gradient GEMM's fp8 operand dZ^T")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--nvtx", action="store_true",
@@ -468,10 +468,12 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "fp8(e4m3/e5m2) x fp8 -> fp32 accumulate", "data": "synthetic",
             "config": {"workload": (WORKLOAD if default_size else "linear_train_step_m%d_k%d_n%d_bias_gelu" % (m, k, n))
                        + {"block128": "", "mx": "_mxfp8", "tensor": "_per_tensor_delayed"}[args.recipe]
-                       + ("_bgrad_from_operand" if args.recipe == "block128" and args.bias_grad == "operand" else ""),
+                       + ({"cast": "", "dgrad": "_bgrad_in_dgrad_epilogue", "operand": "_bgrad_from_operand"}[
+                           args.bias_grad]
+                          if args.recipe == "block128" else ""),
                        "m_tokens": m, "k_in": k, "n_out": n,
                        "acc_mode": args.acc if args.recipe == "block128" else None, "recipe": args.recipe,
-                       "bias_grad": args.bias_grad if args.recipe == "block128" else "dgrad",
+                       "bias_grad": args.bias_grad if args.recipe == "block128" else "dgrad epilogue",
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
@@ -481,7 +483,7 @@ def run_ours(args):
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),
                          "traffic": measured_traffic()
-                         if default_size and args.recipe == "block128" and args.bias_grad == "dgrad" else None,
+                         if default_size and args.recipe == "block128" and args.bias_grad == "cast" else None,
                          "traffic_unit": "bytes",
                          "avg_gemm_ms": avg_gemm_ms},
             "e2e": e2e,
@@ -626,6 +628,14 @@ def run_kernel_study(args):
     db = torch.empty((n,), dtype=torch.float32, device="cuda")
     out["reduce_gbs"] = {"bgrad_from_operand_e5m2_%dx%d" % (n, m): n * (m + 4.0 * m / 128 + 4) / 1e6 / graph_timed(
         lambda: fp8.bgrad_from_operand(DZT, out=db))}
+    # dZ's transposed cast alone and with the bias-gradient sums (+ their
+    # finalize launch), as the step runs them; algorithmic bytes of the cast
+    gbz = m * n * (3.0 + 4.0 / 128) / 1e6
+    wsz = torch.empty((fp8.workspace_size(m, n) // 4,), dtype=torch.float32, device="cuda")
+    out["cast_gbs"]["transposed_e5m2_%dx%d" % (m, n)] = gbz / graph_timed(
+        lambda: fp8.quantize(dZ, fp8.E5M2, transpose=True, out=DZT))
+    out["cast_gbs"]["transposed_dbias_e5m2_%dx%d" % (m, n)] = gbz / graph_timed(
+        lambda: fp8.quantize_dbias(dZ, fp8.E5M2, out_t=DZT, dbias=db, workspace=wsz))
     dW = torch.zeros((n, k), device="cuda")
     out["gemm_tflops"]["wgrad_accumulate_m%d_n%d_k%d" % (n, k, m)] = f / timed(lambda: fp8.gemm_wgrad(DZT, XT, dW))
     for (M, N, K) in ((16384, 7168, 8192), (8192, 8192, 16384)):

@@ -27,7 +27,7 @@ EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", 
            "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
            "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize",
            "fp8_amax_history_update", "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
-           "fp8_bgrad_from_operand")
+           "fp8_bgrad_from_operand", "fp8_quantize_dbias")
 
 
 class Fp8Error(RuntimeError):
@@ -95,11 +95,12 @@ def lib():
         L.fp8_tensor_gemm_dgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp, vp, vp, sz, vp]
         L.fp8_tensor_gemm_wgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp]
         L.fp8_bgrad_from_operand.argtypes = [i64, i64, op, vp, i32, vp]
+        L.fp8_quantize_dbias.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, i64, vp, vp, sz, vp]
         for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
                      "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
                      "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize", "fp8_amax_history_update",
                      "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
-                     "fp8_grouped_wgrad", "fp8_bgrad_from_operand", "fp8_get_device_status",
+                     "fp8_grouped_wgrad", "fp8_bgrad_from_operand", "fp8_quantize_dbias", "fp8_get_device_status",
                      "fp8_debug_starve_next_gemm"):
             getattr(L, name).restype = i32
         _lib = L
@@ -268,6 +269,32 @@ def bgrad_from_operand(A: Fp8Tensor, out: Optional[torch.Tensor] = None, accumul
     _check(lib().fp8_bgrad_from_operand(A.rows, A.k, ctypes.byref(oa), _ptr(out), int(bool(accumulate)), _stream()),
            "fp8_bgrad_from_operand")
     return out
+
+
+def quantize_dbias(x: torch.Tensor, fmt: int, out_t: Optional[Fp8Tensor] = None, out: Optional[Fp8Tensor] = None,
+                   rows: bool = False, dbias: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None) -> Tuple[Optional[Fp8Tensor], Fp8Tensor, torch.Tensor]:
+    """bf16 gradient [rows][cols] -> (row cast or None, transposed cast, db):
+    the transposed cast of quantize(x, fmt, transpose=True) (with rows=True
+    or `out` given, also the row cast) and db [cols] fp32 = the column sums
+    of x, from one read of x."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    if out_t is None:
+        out_t = empty_fp8(C, R, fmt, x.device)
+    if out is None and rows:
+        out = empty_fp8(R, C, fmt, x.device)
+    if dbias is None:
+        dbias = torch.empty((C,), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty((max(R // 128, 1) * C,), dtype=torch.float32, device=x.device)
+    assert dbias.dtype == torch.float32 and dbias.is_contiguous() and tuple(dbias.shape) == (C,)
+    _check(lib().fp8_quantize_dbias(_ptr(x), R, C, x.stride(0), int(fmt), _ptr(out_t.q), _ptr(out_t.scale),
+                                    out_t.scale.stride(0), _ptr(out.q) if out is not None else None,
+                                    _ptr(out.scale) if out is not None else None,
+                                    out.scale.stride(0) if out is not None else 0, _ptr(dbias), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream()), "fp8_quantize_dbias")
+    return out, out_t, dbias
 
 
 def device_status() -> int:

@@ -497,6 +497,47 @@ int fp8_bgrad_from_operand(int64_t rows, int64_t K, const fp8ll_operand_t* A, fl
                : FP8LL_ERR_LAUNCH;
 }
 
+int fp8_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
+                       float* scale_cols, int64_t scale_ld_cols, uint8_t* q_rows, float* scale_rows,
+                       int64_t scale_ld_rows, float* dbias, void* workspace, size_t workspace_bytes,
+                       fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !valid_fmt(fmt)) return FP8LL_ERR_INVALID_ARG;
+    if (cols == 0) return FP8LL_OK;
+    if (!dbias || (reinterpret_cast<uintptr_t>(dbias) & 3u) != 0 || cols > (1LL << 31) - 1)
+        return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    if (rows == 0) {  // a sum over no rows
+        int rc = current_device(&dev);
+        if (rc != FP8LL_OK) return rc;
+        return cudaMemsetAsync(dbias, 0, static_cast<size_t>(cols) * 4, reinterpret_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+                   ? FP8LL_OK
+                   : FP8LL_ERR_LAUNCH;
+    }
+    if (!x_bf16 || !aligned16(x_bf16) || !q_cols || !aligned16(q_cols) || !scale_cols || !aligned16(scale_cols))
+        return FP8LL_ERR_INVALID_ARG;
+    if (ldx < cols || ldx % 8 != 0 || rows % 128 != 0 || rows / 128 > 65535 || rows > (1LL << 31) - 1)
+        return FP8LL_ERR_INVALID_ARG;
+    if (cols % 8 != 0 || scale_ld_cols < cols || scale_ld_cols % 4 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (q_rows) {
+        if (!aligned16(q_rows) || !scale_rows || !aligned16(scale_rows) || cols % 128 != 0 ||
+            scale_ld_rows < rows || scale_ld_rows % 4 != 0)
+            return FP8LL_ERR_INVALID_ARG;
+    }
+    const int64_t part_bytes = (rows / 128) * cols * 4;
+    if (!workspace || !aligned16(workspace) || static_cast<int64_t>(workspace_bytes) < part_bytes)
+        return FP8LL_ERR_WORKSPACE;
+    // the finalize reads the partials while it writes dbias
+    if (overlaps(dbias, cols * 4, workspace, part_bytes)) return FP8LL_ERR_INVALID_ARG;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_quantize_dbias(x_bf16, rows, cols, ldx, fmt, q_cols, scale_cols, scale_ld_cols, q_rows, scale_rows,
+                                 scale_ld_rows, static_cast<float*>(workspace), dbias,
+                                 reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
 int fp8_get_device_status(fp8ll_stream_t stream) {
     DeviceInfo* dev = nullptr;
     int rc = current_device(&dev);

@@ -13,6 +13,11 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
 int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
                          float* scale_rows, int64_t sld_rows, uint8_t* q_cols, float* scale_cols, int64_t sld_cols,
                          cudaStream_t stream);
+// transposed cast (and, with q_rows, the row cast too) of x plus db = column sums of x:
+// partials [rows/128][cols] in dpart, then the fixed-order finalize into dbias
+int launch_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
+                          float* scale_cols, int64_t sld_cols, uint8_t* q_rows, float* scale_rows, int64_t sld_rows,
+                          float* dpart, float* dbias, cudaStream_t stream, int num_sms);
 int launch_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, float* amax, cudaStream_t stream,
                        int num_sms);
 int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,

@@ -153,15 +153,25 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // the fprop should use fast accumulation" scales whole tensors): no block amax,
 // `scale` receives the single scale (written by the first CTA), sr is unused,
 // and when amax_out is given the CTA folds max|x| of its tile into it.
+// With DBIAS the cast also takes the bias gradient of x's columns (the
+// gradient at the layer's pre-activation, cast down its columns for the
+// weight gradient): db = sum over rows of x ("Replaced cublasLt calls with
+// rocblas gemm + 6 manually crafted epilogues", db = sum(dY, axis=0), taken
+// from the high-precision values before the fp8 rounding).  The amax pass adds
+// each thread's 32 values of a column in row order, the quad combines its four
+// parts with the amax pass's shuffles, and one lane writes the tile's partial
+// sum to dpart[blockIdx.y][c]; a finalize adds the row blocks in a fixed order.
 // Three CTAs per SM for the plain transposed cast (64 registers for four
 // spilled; three measured 7% faster), four for the two-way cast (faster there).
-template <int FMT, bool ROWS, bool TENSOR>
+template <int FMT, bool ROWS, bool TENSOR, bool DBIAS = false>
 __global__ void __launch_bounds__(256, ROWS ? 4 : 3) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
                                                             float* __restrict__ scale, int64_t sld,
                                                             uint8_t* __restrict__ qr, float* __restrict__ sr,
                                                             int64_t sldr, const float* __restrict__ amax_in,
-                                                            unsigned* __restrict__ amax_out) {
+                                                            unsigned* __restrict__ amax_out,
+                                                            float* __restrict__ dpart = nullptr) {
+    static_assert(!(DBIAS && TENSOR), "the bias-gradient sums ride on the block-amax pass");
     __shared__ __align__(16) uint32_t tile[128][64];
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
@@ -234,19 +244,34 @@ __global__ void __launch_bounds__(256, ROWS ? 4 : 3) quantize_cols_kernel(const 
     float inv_lo = inv_t, s_lo = s_t, inv_hi = inv_t, s_hi = s_t;
     if (!TENSOR) {
         float amax_lo = 0.0f, amax_hi = 0.0f;
+        float sum_lo = 0.0f, sum_hi = 0.0f;  // DBIAS
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
             amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
             amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
+            if (DBIAS) {
+                sum_lo = __fadd_rn(sum_lo, bf16_lo(w));
+                sum_hi = __fadd_rn(sum_hi, bf16_hi(w));
+            }
         }
 #pragma unroll
         for (int off = 1; off <= 2; off <<= 1) {
             amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
             amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
+            if (DBIAS) {
+                // a + b on one lane, b + a on its partner: the same bits on all four
+                sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, off));
+                sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, off));
+            }
         }
         block_scale<FMT>(amax_lo, inv_lo, s_lo);
         block_scale<FMT>(amax_hi, inv_hi, s_hi);
+        if (DBIAS && p == 0 && c < cols) {
+            // cols is even: c + 1 < cols too
+            dpart[static_cast<int64_t>(blockIdx.y) * cols + c] = sum_lo;
+            dpart[static_cast<int64_t>(blockIdx.y) * cols + c + 1] = sum_hi;
+        }
     }
     if (c < cols) {
         uint32_t wl[8], wh[8];
@@ -578,6 +603,30 @@ int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                                                         sld_cols, q_rows, scale_rows, sld_rows,
                                                                         nullptr, nullptr);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
+                          float* scale_cols, int64_t sld_cols, uint8_t* q_rows, float* scale_rows, int64_t sld_rows,
+                          float* dpart, float* dbias, cudaStream_t stream, int num_sms) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+    if (q_rows) {
+        if (fmt == 0)
+            quantize_cols_kernel<0, true, false, true><<<grid, 256, 0, stream>>>(
+                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows, scale_rows, sld_rows, nullptr, nullptr, dpart);
+        else
+            quantize_cols_kernel<1, true, false, true><<<grid, 256, 0, stream>>>(
+                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows, scale_rows, sld_rows, nullptr, nullptr, dpart);
+    } else {
+        if (fmt == 0)
+            quantize_cols_kernel<0, false, false, true><<<grid, 256, 0, stream>>>(
+                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, nullptr, nullptr, 0, nullptr, nullptr, dpart);
+        else
+            quantize_cols_kernel<1, false, false, true><<<grid, 256, 0, stream>>>(
+                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, nullptr, nullptr, 0, nullptr, nullptr, dpart);
+    }
+    if (cudaGetLastError() != cudaSuccess) return -3;
+    return launch_bgrad_finalize(dpart, rows / 128, cols, dbias, stream, num_sms);
 }
 
 static int grid_rows(int64_t rows, int num_sms) {

@@ -33,16 +33,18 @@ from . import binding as B
 
 class LinearTrainStep:
     def __init__(self, m: int, k: int, n: int, device="cuda", acc_mode: int = B.ACC_FULL,
-                 input_grad: bool = False, bias_grad: str = "dgrad"):
-        """``bias_grad`` picks where db comes from: "dgrad" sums the fp32 dZ in
-        the data-gradient GEMM's epilogue (before any fp8 rounding); "operand"
-        reduces the weight-gradient GEMM's fp8 operand dZ^T over the tokens
-        (the BGRADB form: db taken together with dW from the gradient operand,
-        "Replaced cublasLt calls with rocblas gemm + 6 manually crafted
-        epilogues"), after a data-gradient GEMM without the sums."""
+                 input_grad: bool = False, bias_grad: str = "cast"):
+        """``bias_grad`` picks where db = sum(dZ, axis=0) comes from ("Replaced
+        cublasLt calls with rocblas gemm + 6 manually crafted epilogues" takes
+        it by reducing the stored gradient): "cast" (the default) sums the
+        bf16 dZ in its transposed cast for the weight gradient, from the same
+        read; "dgrad" sums the fp32 dZ in the data-gradient GEMM's epilogue,
+        before its bf16 rounding; "operand" reduces the weight-gradient GEMM's
+        fp8 operand dZ^T over the tokens (the BGRADB form).  With "cast" and
+        "operand" the data-gradient GEMM runs without its column sums."""
         assert m % 128 == 0 and k % 128 == 0
         assert not input_grad or n % 128 == 0, "the two-way casts of W and dZ need n % 128 == 0"
-        assert bias_grad in ("dgrad", "operand")
+        assert bias_grad in ("dgrad", "cast", "operand")
         self.m, self.k, self.n = m, k, n
         self.acc_mode = acc_mode
         self.bias_grad = bias_grad
@@ -109,7 +111,14 @@ class LinearTrainStep:
         else:
             cast_dz = ("quantize", lambda: B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq))
         plan = [("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq))]
-        if self.bias_grad == "operand":
+        if self.bias_grad == "cast":
+            dzq = self.dZq if self.with_input_grad else None
+            plan += [
+                ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, self.acc_mode, out=self.dZ)),
+                ("quantize", lambda: B.quantize_dbias(self.dZ, B.E5M2, out_t=self.dZTq, out=dzq, dbias=self.db,
+                                                      workspace=self.ws)),
+            ]
+        elif self.bias_grad == "operand":
             plan += [
                 ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, self.acc_mode, out=self.dZ)),
                 cast_dz,
@@ -161,7 +170,7 @@ class LinearTrainStep:
         return self._forward_plan(X, W, b) + self._backward_plan(X, dY)
 
     # 4 casts (3 with a cached weight) + fprop GEMM + dgrad GEMM + bias-gradient finalize (or the
-    # reduction of dZ^T's codes) + wgrad GEMM
+    # reduction of dZ^T's codes) + wgrad GEMM; with bias_grad="cast" the finalize follows the cast
     @property
     def KERNELS_PER_STEP(self):
         return 7 if self.weight_cached else 8

@@ -7,6 +7,7 @@
  *
  *   fp8_quantize        bf16 -> e4m3 / e5m2 codes + block scales
  *   fp8_quantize_dual   both orientations of that cast from one read
+ *   fp8_quantize_dbias  the transposed cast of a gradient with its bias gradient
  *   fp8_mx_*            the MXFP8 variant (power-of-two scales per 32 values)
  *   fp8_tensor_*        per-tensor scaling (current or delayed amax)
  *   fp8_gemm_fprop      C = A B^T with bias / tanh-GELU epilogues, bf16 out
@@ -222,6 +223,25 @@ int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
  *   1 <= G <= 256.  A.ld_q, B.ld_q >= sum of k_sizes. */
 int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const fp8ll_operand_t* A,
                       const fp8ll_operand_t* B, float* out, int accumulate, int acc_mode, fp8ll_stream_t stream);
+
+/* The transposed cast of a gradient together with its bias gradient (db =
+ * sum(dY, axis=0) of "Replaced cublasLt calls with rocblas gemm + 6 manually
+ * crafted epilogues", taken from the bf16 values while they are cast for the
+ * weight-gradient GEMM, so the data-gradient GEMM needs no column sums):
+ *   q_cols / scale_cols: exactly fp8_quantize(x, ..., transpose = 1) -- codes
+ *     [cols][rows], scales [rows/128][scale_ld_cols];
+ *   q_rows / scale_rows: NULL, or exactly the row cast (fp8_quantize_dual's
+ *     row outputs; needs cols % 128 == 0);
+ *   dbias: fp32 [cols], dbias[c] = sum over all rows of x[r][c].
+ * rows % 128 == 0, cols % 8 == 0, ldx >= cols, ldx % 8 == 0.  rows == 0 sets
+ * dbias to zero.  workspace: >= (rows/128) * cols * 4 bytes, 16-byte aligned
+ * (fp8_workspace_size(rows, cols) is enough), else FP8LL_ERR_WORKSPACE; it
+ * holds per-128-row partial sums and may not overlap dbias.  The sums run in
+ * fp32 in a fixed order (each 128-row block, then the blocks): deterministic. */
+int fp8_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
+                       float* scale_cols, int64_t scale_ld_cols, uint8_t* q_rows, float* scale_rows,
+                       int64_t scale_ld_rows, float* dbias, void* workspace, size_t workspace_bytes,
+                       fp8ll_stream_t stream);
 
 /* Bias gradient reduced from the weight-gradient GEMM's gradient operand
  * (the BGRADB epilogue on "Replaced cublasLt calls with rocblas gemm + 6

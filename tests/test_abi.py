@@ -170,3 +170,35 @@ def test_bgrad_from_operand_validation(L):
     assert fn(8, 256, ctypes.byref(op), vp(q - 28), 0, None) == E  # db's last element on the first code
     assert fn(0, 256, ctypes.byref(op), None, 0, None) == f.binding.OK  # no rows: nothing to do
     assert fn(-1, 256, ctypes.byref(op), vp(0x300000), 0, None) == E
+
+
+def test_quantize_dbias_validation(L):
+    import fp8_linear_layer_gb300 as f
+    E, WS = f.binding.ERR_INVALID_ARG, f.binding.ERR_WORKSPACE
+    vp = ctypes.c_void_p
+    x, q, s, db, ws = vp(0x100000), vp(0x200000), vp(0x300000), vp(0x400000), vp(0x500000)
+    fn = L.fp8_quantize_dbias
+    need = 2 * 64 * 4  # (256/128) x 64 floats
+    assert fn(x, 200, 64, 64, 1, q, s, 64, None, None, 0, db, ws, need, None) == E  # rows % 128
+    assert fn(x, 256, 60, 64, 1, q, s, 64, None, None, 0, db, ws, need, None) == E  # cols % 8
+    assert fn(x, 256, 64, 64, 1, q, s, 60, None, None, 0, db, ws, need, None) == E  # scale_ld < cols
+    assert fn(x, 256, 64, 64, 1, q, s, 64, q, s, 256, db, ws, need, None) == E  # row cast needs cols % 128
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, vp(0x400002), ws, need, None) == E  # db misaligned
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, db, ws, need - 4, None) == WS
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, db, None, need, None) == WS
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, vp(0x500000 + 64), ws, need, None) == E  # db in ws
+    assert fn(x, 256, 0, 64, 1, q, s, 64, None, None, 0, db, ws, need, None) == f.binding.OK  # no columns
+    assert fn(x, 256, 64, 64, 2, q, s, 64, None, None, 0, db, ws, need, None) == E  # format
+
+
+def test_binding_checks_every_status_with_its_call_name():
+    # each _check(status, name) call passes exactly those two arguments
+    import ast
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "fp8_linear_layer_gb300",
+                        "binding.py")
+    calls = [n for n in ast.walk(ast.parse(open(path).read()))
+             if isinstance(n, ast.Call) and getattr(n.func, "id", "") == "_check"]
+    assert len(calls) >= 20
+    for c in calls:
+        assert len(c.args) == 2 and isinstance(c.args[1], ast.Constant), c.lineno
+        assert c.args[1].value.startswith("fp8_"), c.lineno

@@ -138,7 +138,7 @@ def test_writes_stay_in_bounds(fp8):
 def test_train_step_with_the_operand_bias_gradient(fp8):
     """LinearTrainStep(bias_grad="operand"): the data-gradient GEMM drops its
     bias-gradient sums and db is reduced from dZ^T's codes.  dZ and dW are
-    bit-identical to the default step's; db is the oracle's column sum of its
+    bit-identical to the step with the epilogue's sums; db is the oracle's column sum of its
     dZ within one e5m2 rounding per element (plus dZ's own bound)."""
     import oracle
     from fp8_linear_layer_gb300.linear import LinearTrainStep
@@ -149,7 +149,7 @@ def test_train_step_with_the_operand_bias_gradient(fp8):
     b = workloads.normal_bf16((n,), 79, "b", std=0.02)
     dY = workloads.normal_bf16((m, k), 79, "dY", std=1e-2)
     args = (X.cuda(), W.cuda(), b.cuda(), dY.cuda())
-    ref = LinearTrainStep(m, k, n)
+    ref = LinearTrainStep(m, k, n, bias_grad="dgrad")
     st = LinearTrainStep(m, k, n, bias_grad="operand")
     assert st.KERNELS_PER_STEP == ref.KERNELS_PER_STEP == 8
     assert [kind for kind, _ in st.launches(*args)].count("reduce") == 1

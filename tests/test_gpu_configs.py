@@ -171,7 +171,7 @@ def test_train_step_chain_small(fp8):
     W = workloads.normal_bf16((n, k), 77, "W", std=0.05)
     b = workloads.normal_bf16((n,), 77, "b", std=0.02)
     dY = workloads.normal_bf16((m, k), 77, "dY", std=1e-2)
-    st = LinearTrainStep(m, k, n)
+    st = LinearTrainStep(m, k, n, bias_grad="dgrad")  # the epilogue's column sums
     st.step(X.cuda(), W.cuda(), b.cuda(), dY.cuda())
     torch.cuda.synchronize()
     assert fp8.device_status() == 0
