@@ -391,7 +391,9 @@ def run_ours(args):
     X, W, b, dY = (t.to(dev, non_blocking=True) for t in (hX, hW, hb, hdY))
     if args.recipe == "mx":
         from fp8_linear_layer_gb300.linear import MxLinearTrainStep
-        step = MxLinearTrainStep(m, k, n, dev)
+        if args.bias_grad == "operand":
+            raise SystemExit("--bias-grad operand reduces 1x128-scaled operands only")
+        step = MxLinearTrainStep(m, k, n, dev, bias_grad=args.bias_grad)
     elif args.recipe == "tensor":
         from fp8_linear_layer_gb300.linear import TensorLinearTrainStep
         step = TensorLinearTrainStep(m, k, n, dev)
@@ -470,10 +472,10 @@ def run_ours(args):
                        + {"block128": "", "mx": "_mxfp8", "tensor": "_per_tensor_delayed"}[args.recipe]
                        + ({"cast": "", "dgrad": "_bgrad_in_dgrad_epilogue", "operand": "_bgrad_from_operand"}[
                            args.bias_grad]
-                          if args.recipe == "block128" else ""),
+                          if args.recipe in ("block128", "mx") else ""),
                        "m_tokens": m, "k_in": k, "n_out": n,
                        "acc_mode": args.acc if args.recipe == "block128" else None, "recipe": args.recipe,
-                       "bias_grad": args.bias_grad if args.recipe == "block128" else "dgrad epilogue",
+                       "bias_grad": getattr(step, "bias_grad", "dgrad"),
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},

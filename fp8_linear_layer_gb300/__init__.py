@@ -14,7 +14,7 @@ from .binding import (ACC_FAST, ACC_FULL, E4M3, E5M2, EPI_BIAS, EPI_BIAS_GELU, E
                       scale_ld, status_string, workspace_size, Fp8MxTensor, empty_mx, mx_gemm_dgrad, mx_gemm_fprop,
                       mx_gemm_wgrad, mx_quantize, mx_sf_bytes, Fp8TensorScaled, amax_history_update,
                       empty_tensor_scaled, tensor_amax, tensor_gemm_dgrad, tensor_gemm_fprop, tensor_gemm_wgrad,
-                      tensor_quantize, bgrad_from_operand, quantize_dbias)
+                      tensor_quantize, bgrad_from_operand, quantize_dbias, mx_quantize_dbias)
 
 __all__ = ["ACC_FAST", "ACC_FULL", "E4M3", "E5M2", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_DGELU", "EPI_DGELU_BGRAD",
            "EPI_NONE", "EXPORTS", "Fp8Error", "Fp8Tensor", "cast_f32", "debug_starve_next_gemm", "device_status",
@@ -22,4 +22,4 @@ __all__ = ["ACC_FAST", "ACC_FULL", "E4M3", "E5M2", "EPI_BIAS", "EPI_BIAS_GELU", 
            "status_string", "workspace_size", "Fp8MxTensor", "empty_mx", "mx_gemm_dgrad", "mx_gemm_fprop",
            "mx_gemm_wgrad", "mx_quantize", "mx_sf_bytes", "Fp8TensorScaled", "amax_history_update",
            "empty_tensor_scaled", "tensor_amax", "tensor_gemm_dgrad", "tensor_gemm_fprop", "tensor_gemm_wgrad",
-           "tensor_quantize", "bgrad_from_operand", "quantize_dbias"]
+           "tensor_quantize", "bgrad_from_operand", "quantize_dbias", "mx_quantize_dbias"]

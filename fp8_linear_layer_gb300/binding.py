@@ -27,7 +27,7 @@ EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", 
            "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
            "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize",
            "fp8_amax_history_update", "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
-           "fp8_bgrad_from_operand", "fp8_quantize_dbias")
+           "fp8_bgrad_from_operand", "fp8_quantize_dbias", "fp8_mx_quantize_dbias")
 
 
 class Fp8Error(RuntimeError):
@@ -96,11 +96,13 @@ def lib():
         L.fp8_tensor_gemm_wgrad.argtypes = [i64, i64, i64, top, top, vp, i32, vp]
         L.fp8_bgrad_from_operand.argtypes = [i64, i64, op, vp, i32, vp]
         L.fp8_quantize_dbias.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, i64, vp, vp, sz, vp]
+        L.fp8_mx_quantize_dbias.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]
         for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
                      "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
                      "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize", "fp8_amax_history_update",
                      "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
-                     "fp8_grouped_wgrad", "fp8_bgrad_from_operand", "fp8_quantize_dbias", "fp8_get_device_status",
+                     "fp8_grouped_wgrad", "fp8_bgrad_from_operand", "fp8_quantize_dbias", "fp8_mx_quantize_dbias",
+                     "fp8_get_device_status",
                      "fp8_debug_starve_next_gemm"):
             getattr(L, name).restype = i32
         _lib = L
@@ -349,6 +351,26 @@ def mx_quantize(x: torch.Tensor, fmt: int, transpose: bool = False, out: Optiona
     _check(lib().fp8_mx_quantize(_ptr(x), rows, cols, x.stride(0), int(fmt), int(bool(transpose)), _ptr(out.q),
                                  _ptr(out.sf), _stream()), "fp8_mx_quantize")
     return out
+
+
+def mx_quantize_dbias(x: torch.Tensor, fmt: int, out: Optional[Fp8MxTensor] = None,
+                      dbias: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None) -> Tuple[Fp8MxTensor, torch.Tensor]:
+    """bf16 gradient [rows][cols] -> (mx_quantize(x, fmt, transpose=True), db):
+    db [cols] fp32 = the column sums of x, from the same read."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    if out is None:
+        out = empty_mx(C, R, fmt, x.device)
+    if dbias is None:
+        dbias = torch.empty((C,), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty((max(R // 128, 1) * C,), dtype=torch.float32, device=x.device)
+    assert dbias.dtype == torch.float32 and dbias.is_contiguous() and tuple(dbias.shape) == (C,)
+    _check(lib().fp8_mx_quantize_dbias(_ptr(x), R, C, x.stride(0), int(fmt), _ptr(out.q), _ptr(out.sf), _ptr(dbias),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(), _stream()),
+           "fp8_mx_quantize_dbias")
+    return out, dbias
 
 
 def mx_gemm_fprop(A: Fp8MxTensor, B: Fp8MxTensor, bias: Optional[torch.Tensor] = None, epi: int = EPI_BIAS_GELU,

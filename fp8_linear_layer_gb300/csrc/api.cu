@@ -538,6 +538,37 @@ int fp8_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t l
                : FP8LL_ERR_LAUNCH;
 }
 
+int fp8_mx_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q,
+                          uint8_t* sf, float* dbias, void* workspace, size_t workspace_bytes, fp8ll_stream_t stream) {
+    if (rows < 0 || cols < 0 || !valid_fmt(fmt)) return FP8LL_ERR_INVALID_ARG;
+    if (cols == 0) return FP8LL_OK;
+    if (!dbias || (reinterpret_cast<uintptr_t>(dbias) & 3u) != 0 || cols > (1LL << 31) - 1)
+        return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    if (rows == 0) {  // a sum over no rows
+        int rc = current_device(&dev);
+        if (rc != FP8LL_OK) return rc;
+        return cudaMemsetAsync(dbias, 0, static_cast<size_t>(cols) * 4, reinterpret_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+                   ? FP8LL_OK
+                   : FP8LL_ERR_LAUNCH;
+    }
+    if (!x_bf16 || !q || !sf || !aligned16(x_bf16) || !aligned16(q) || !aligned16(sf)) return FP8LL_ERR_INVALID_ARG;
+    if (ldx < cols || ldx % 8 != 0 || rows % 128 != 0 || cols % 8 != 0 || rows / 128 > 65535 ||
+        rows > (1LL << 31) - 1)
+        return FP8LL_ERR_INVALID_ARG;
+    const int64_t part_bytes = (rows / 128) * cols * 4;
+    if (!workspace || !aligned16(workspace) || static_cast<int64_t>(workspace_bytes) < part_bytes)
+        return FP8LL_ERR_WORKSPACE;
+    if (overlaps(dbias, cols * 4, workspace, part_bytes)) return FP8LL_ERR_INVALID_ARG;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    return launch_mx_quantize_dbias(x_bf16, rows, cols, ldx, fmt, q, sf, static_cast<float*>(workspace), dbias,
+                                    reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
 int fp8_get_device_status(fp8ll_stream_t stream) {
     DeviceInfo* dev = nullptr;
     int rc = current_device(&dev);

@@ -18,6 +18,9 @@ int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx,
 int launch_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
                           float* scale_cols, int64_t sld_cols, uint8_t* q_rows, float* scale_rows, int64_t sld_rows,
                           float* dpart, float* dbias, cudaStream_t stream, int num_sms);
+// MXFP8 transposed cast of x plus db = column sums of x (partials in dpart, then the finalize)
+int launch_mx_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q,
+                             uint8_t* sf, float* dpart, float* dbias, cudaStream_t stream, int num_sms);
 int launch_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, float* amax, cudaStream_t stream,
                        int num_sms);
 int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, const float* amax_in,

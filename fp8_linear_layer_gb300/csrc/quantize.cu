@@ -478,10 +478,15 @@ __global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const uint16_t* _
 
 // Transposed: the 1x128 kernel's staged 128 x 128 tile; a thread's 32 rows of
 // a column are exactly one MX group (group p of the 128-token block).
-template <int FMT>
+// With DBIAS the cast also adds each thread's 32 values of a column (one MX
+// block) in row order and combines the quad's four parts, in the same order as
+// the 1x128 transposed cast, so the per-128-row partials in dpart (and the
+// bias gradient the finalize makes of them) are bit-identical to that cast's.
+template <int FMT, bool DBIAS = false>
 __global__ void __launch_bounds__(256, 3) mx_quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                   int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
-                                                                  uint8_t* __restrict__ sf, int64_t groups) {
+                                                                  uint8_t* __restrict__ sf, int64_t groups,
+                                                                  float* __restrict__ dpart = nullptr) {
     __shared__ __align__(16) uint32_t tile[128][64];
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
@@ -501,11 +506,27 @@ __global__ void __launch_bounds__(256, 3) mx_quantize_cols_kernel(const uint16_t
     const int p = threadIdx.x & 3;
     const int64_t c = c0 + 2 * cp;
     float amax_lo = 0.0f, amax_hi = 0.0f;
+    float sum_lo = 0.0f, sum_hi = 0.0f;  // DBIAS
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
         amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
         amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
+        if (DBIAS) {
+            sum_lo = __fadd_rn(sum_lo, bf16_lo(w));
+            sum_hi = __fadd_rn(sum_hi, bf16_hi(w));
+        }
+    }
+    if (DBIAS) {
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, off));
+            sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, off));
+        }
+        if (p == 0 && c < cols) {  // cols is even: c + 1 < cols too
+            dpart[static_cast<int64_t>(blockIdx.y) * cols + c] = sum_lo;
+            dpart[static_cast<int64_t>(blockIdx.y) * cols + c + 1] = sum_hi;
+        }
     }
     const int e_lo = mx_exponent<FMT>(amax_lo), e_hi = mx_exponent<FMT>(amax_hi);
     const float inv_lo = mx_inverse_scale(e_lo), inv_hi = mx_inverse_scale(e_hi);
@@ -725,6 +746,24 @@ int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, i
             mx_quantize_cols_kernel<1><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_mx_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q,
+                             uint8_t* sf, float* dpart, float* dbias, cudaStream_t stream, int num_sms) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    const int64_t groups = mx_sf_groups(cols);
+    if (cols % 256 != 0) {
+        // rows beyond the matrix in the last group pair read as scale 1
+        if (cudaMemsetAsync(sf, 127, static_cast<size_t>(rows / 128) * groups * 512, stream) != cudaSuccess)
+            return -3;
+    }
+    dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+    if (fmt == 0)
+        mx_quantize_cols_kernel<0, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups, dpart);
+    else
+        mx_quantize_cols_kernel<1, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, sf, groups, dpart);
+    if (cudaGetLastError() != cudaSuccess) return -3;
+    return launch_bgrad_finalize(dpart, rows / 128, cols, dbias, stream, num_sms);
 }
 
 int launch_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, cudaStream_t stream, int num_sms) {

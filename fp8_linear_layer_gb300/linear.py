@@ -182,9 +182,13 @@ class MxLinearTrainStep(LinearTrainStep):
     apply them (no software promotion).  Same buffers for the outputs; 9
     launches per step (X is cast once per orientation)."""
 
-    def __init__(self, m: int, k: int, n: int, device="cuda"):
+    def __init__(self, m: int, k: int, n: int, device="cuda", bias_grad: str = "cast"):
+        """``bias_grad``: "cast" (default) takes db in dZ's transposed cast,
+        "dgrad" in the data-gradient GEMM's epilogue (as LinearTrainStep)."""
         assert m % 128 == 0 and k % 128 == 0
+        assert bias_grad in ("cast", "dgrad")
         self.m, self.k, self.n = m, k, n
+        self.bias_grad = bias_grad
         self.acc_mode = B.ACC_FULL
         dev = torch.device(device)
         self.Xq = B.empty_mx(m, k, B.E4M3, dev)
@@ -207,11 +211,19 @@ class MxLinearTrainStep(LinearTrainStep):
         ]
 
     def _backward_plan(self, X, dY):
-        return [
-            ("quantize", lambda: B.mx_quantize(dY, B.E5M2, out=self.dYq)),
-            ("gemm", lambda: B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ,
-                                             bgrad=self.db, workspace=self.ws)),
-            ("quantize", lambda: B.mx_quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)),
+        if self.bias_grad == "cast":
+            dz = [
+                ("gemm", lambda: B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, out=self.dZ)),
+                ("quantize", lambda: B.mx_quantize_dbias(self.dZ, B.E5M2, out=self.dZTq, dbias=self.db,
+                                                         workspace=self.ws)),
+            ]
+        else:
+            dz = [
+                ("gemm", lambda: B.mx_gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU_BGRAD, out=self.dZ,
+                                                 bgrad=self.db, workspace=self.ws)),
+                ("quantize", lambda: B.mx_quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq)),
+            ]
+        return [("quantize", lambda: B.mx_quantize(dY, B.E5M2, out=self.dYq))] + dz + [
             ("quantize", lambda: B.mx_quantize(X, B.E4M3, transpose=True, out=self.XTq)),
             ("gemm", lambda: B.mx_gemm_wgrad(self.dZTq, self.XTq, self.dW, accumulate=True)),
         ]

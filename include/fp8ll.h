@@ -313,6 +313,16 @@ int fp8_mx_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
 int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const fp8ll_mx_operand_t* B,
                       float* out, int accumulate, fp8ll_stream_t stream);
 
+/* fp8_mx_quantize(x, ..., transpose = 1) together with the bias gradient of
+ * x's columns, dbias[c] = sum over all rows of x[r][c] (as fp8_quantize_dbias,
+ * for the MXFP8 recipe's transposed cast of the gradient).  Codes and scale
+ * bytes are exactly fp8_mx_quantize's; rows % 128 == 0, cols % 8 == 0;
+ * rows == 0 sets dbias to zero.  workspace: >= (rows/128) * cols * 4 bytes,
+ * 16-byte aligned, not overlapping dbias.  The sums run in the same fixed order
+ * as fp8_quantize_dbias's, so the two give the same bits for the same x. */
+int fp8_mx_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q,
+                          uint8_t* sf, float* dbias, void* workspace, size_t workspace_bytes, fp8ll_stream_t stream);
+
 /* ---- per-tensor scaling ----------------------------------------------------
  * "FP8 GEMM for the fprop should use fast accumulation" casts whole tensors
  * with one scale each.  The cast takes the amax to scale with from the caller:

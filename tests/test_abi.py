@@ -202,3 +202,19 @@ def test_binding_checks_every_status_with_its_call_name():
     for c in calls:
         assert len(c.args) == 2 and isinstance(c.args[1], ast.Constant), c.lineno
         assert c.args[1].value.startswith("fp8_"), c.lineno
+
+
+def test_mx_quantize_dbias_validation(L):
+    import fp8_linear_layer_gb300 as f
+    E, WS = f.binding.ERR_INVALID_ARG, f.binding.ERR_WORKSPACE
+    vp = ctypes.c_void_p
+    x, q, sf, db, ws = vp(0x100000), vp(0x200000), vp(0x300000), vp(0x400000), vp(0x500000)
+    fn = L.fp8_mx_quantize_dbias
+    need = 2 * 64 * 4
+    assert fn(x, 200, 64, 64, 1, q, sf, db, ws, need, None) == E  # rows % 128
+    assert fn(x, 256, 60, 64, 1, q, sf, db, ws, need, None) == E  # cols % 8
+    assert fn(x, 256, 64, 56, 1, q, sf, db, ws, need, None) == E  # ldx < cols
+    assert fn(x, 256, 64, 64, 1, q, sf, vp(0x400001), ws, need, None) == E
+    assert fn(x, 256, 64, 64, 1, q, sf, db, ws, need - 4, None) == WS
+    assert fn(x, 256, 64, 64, 1, q, sf, vp(0x500000 + 256), ws, need, None) == E  # db inside the partials
+    assert fn(x, 256, 0, 64, 1, q, sf, db, ws, need, None) == f.binding.OK
