@@ -41,3 +41,16 @@ def test_reference_arm_line(tmp_path):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_bias_gradient_modes(monkeypatch):
+    # the step's default takes db in dZ's transposed cast; every mode is accepted
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    assert bench.parse_args().bias_grad == "cast"
+    for mode in ("cast", "dgrad", "operand"):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--bias-grad", mode])
+        assert bench.parse_args().bias_grad == mode
+    from fp8_linear_layer_gb300.linear import LinearTrainStep, MxLinearTrainStep
+    import inspect
+    assert inspect.signature(LinearTrainStep.__init__).parameters["bias_grad"].default == "cast"
+    assert inspect.signature(MxLinearTrainStep.__init__).parameters["bias_grad"].default == "cast"
