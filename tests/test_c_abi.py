@@ -41,6 +41,17 @@ int main(void) {
     CHECK(fp8_tensor_gemm_fprop(8, 8, 256, &top, &top, p, FP8LL_EPI_BIAS_GELU, p, NULL, NULL) ==
           FP8LL_ERR_INVALID_ARG);
     CHECK(fp8_amax_history_update((float*)p, 0, 4, (const float*)p, (float*)p, NULL) == FP8LL_ERR_INVALID_ARG);
+    /* the bias-gradient entries: refused on the host, or nothing to do */
+    CHECK(fp8_bgrad_from_operand(8, 200, &op, (float*)p, 0, NULL) == FP8LL_ERR_INVALID_ARG);
+    CHECK(fp8_bgrad_from_operand(0, 256, &op, NULL, 0, NULL) == FP8LL_OK);
+    CHECK(fp8_quantize_dbias(p, 256, 64, 64, FP8LL_E5M2, (uint8_t*)p, (float*)p, 64, NULL, NULL, 0,
+                             (float*)((char*)p + 4096), (char*)p + 8192, 2 * 64 * 4 - 4, NULL) == FP8LL_ERR_WORKSPACE);
+    CHECK(fp8_quantize_dbias(p, 200, 64, 64, FP8LL_E5M2, (uint8_t*)p, (float*)p, 64, NULL, NULL, 0,
+                             (float*)p, p, 1 << 20, NULL) == FP8LL_ERR_INVALID_ARG);
+    CHECK(fp8_mx_quantize_dbias(p, 256, 60, 64, FP8LL_E5M2, (uint8_t*)p, (uint8_t*)p, (float*)p, p, 1 << 20,
+                                NULL) == FP8LL_ERR_INVALID_ARG);
+    CHECK(fp8_mx_quantize_dbias(p, 256, 0, 64, FP8LL_E5M2, (uint8_t*)p, (uint8_t*)p, NULL, NULL, 0, NULL) ==
+          FP8LL_OK);
     printf("ok\n");
     return 0;
 }
