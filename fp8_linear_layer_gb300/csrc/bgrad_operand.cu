@@ -18,6 +18,7 @@
 // exactly and rounds once.  The sums run in a fixed order (four chains of four
 // codes and a tree per 16 bytes, the groups in turn, a butterfly over the
 // lanes, the four warps of a row in turn), so results are deterministic.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -143,14 +144,16 @@ __global__ void __launch_bounds__(kThreadsPerCta) operand_rowsum_kernel(const ui
 template <int FMT>
 int launch_fmt(const uint8_t* q, int64_t ldq, const float* scale, int64_t sld, int64_t rows, int64_t K, float* db,
                int accumulate, cudaStream_t stream, int num_sms) {
-    static int per_sm = 0;  // resident CTAs per SM, from the occupancy calculator once
+    // resident CTAs per SM, from the occupancy calculator once (callers on
+    // several host threads may all compute it: they store the same value)
+    static std::atomic<int> cached{0};
+    int per_sm = cached.load(std::memory_order_relaxed);
     if (per_sm == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, operand_rowsum_kernel<FMT>, kThreadsPerCta, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, operand_rowsum_kernel<FMT>, kThreadsPerCta, 0) !=
                 cudaSuccess ||
-            n < 1)
+            per_sm < 1)
             return -1;
-        per_sm = n;
+        cached.store(per_sm, std::memory_order_relaxed);
     }
     const int64_t npairs = (rows + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t wave = static_cast<int64_t>(num_sms) * per_sm;
