@@ -226,8 +226,8 @@ def cpu_step(xb, wb, bb, dyb):
     qdy, sdy = oracle.quantize(dyb, oracle.E5M2)
     acc2, _ = oracle.gemm(qdy, sdy, oracle.E5M2, qw, sw, oracle.E4M3)
     dZ = oracle.dgrad_epilogue(acc2, zb)
-    oracle.colsum(dZ)
     dzb = oracle.f64_to_bf16_array(dZ)
+    oracle.colsum(oracle.bf16_to_f64(dzb))  # db of the stored bf16 dZ, as the step takes it by default
     qdzt, sdzt = oracle.quantize(dzb, oracle.E5M2, transpose=True)
     qxt, sxt = oracle.quantize(xb, oracle.E4M3, transpose=True)
     oracle.gemm(qdzt, sdzt, oracle.E5M2, qxt, sxt, oracle.E4M3)
