@@ -93,10 +93,12 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx", "tensor"], default=None,
+    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx", "tensor", "casts"],
+                    default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
     ap.add_argument("--study-k", type=int, default=16384)
+    ap.add_argument("--reps", type=int, default=10, help="timed launches per kernel in --study casts")
     return ap.parse_args()
 
 
@@ -476,6 +478,12 @@ def run_ours(args):
                        "m_tokens": m, "k_in": k, "n_out": n,
                        "acc_mode": args.acc if args.recipe == "block128" else None, "recipe": args.recipe,
                        "bias_grad": getattr(step, "bias_grad", "dgrad"),
+                       # what the timed data-gradient GEMM's epilogue does (the per-GEMM
+                       # figure of the bias-gradient epilogue is bench.py --study kernels')
+                       "dgrad_epilogue": "dGELU + bias-gradient column sums"
+                       if getattr(step, "bias_grad", "dgrad") == "dgrad"
+                       else "dGELU only (db taken %s)" % {"cast": "in dZ's transposed cast",
+                                                          "operand": "from dZ^T's fp8 codes"}[step.bias_grad],
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
@@ -661,6 +669,51 @@ def run_kernel_study(args):
     print(json.dumps(out))
 
 
+def run_cast_study(args):
+    """The 1x128 casts on a 32768 x 8192 bf16 matrix, in a fixed order (rows
+    e4m3, rows e5m2, transposed e4m3, transposed e5m2 with the bias-gradient
+    column sums, both orientations e4m3), each launched once untimed and then
+    --reps times between CUDA events; GB/s of algorithmic bytes: 2 read + 1 +
+    4/128 written per element and orientation (+ 4 per column per 128 rows
+    for the column-sum partials).  With --reps 1 every kernel launches twice,
+    so a profiler can take the second launch of each."""
+    import torch
+    import workloads
+    import fp8_linear_layer_gb300 as fp8
+    reps = max(1, args.reps)
+    R, C = 32768, 8192
+    x = workloads.normal_bf16((R, C), SEED + 2, "C").cuda()
+    n = x.numel()
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps
+
+    one = n * (3.0 + 4.0 / 128) / 1e6
+    qr, qt = fp8.empty_fp8(R, C, fp8.E4M3), fp8.empty_fp8(C, R, fp8.E4M3)
+    db = torch.empty((C,), dtype=torch.float32, device="cuda")
+    ws = torch.empty(((R // 128) * C,), dtype=torch.float32, device="cuda")
+    out = {"study": "casts", "reps": reps, "shape": [R, C], "cast_gbs": {}}
+    out["cast_gbs"]["rows_e4m3"] = one / timed(lambda: fp8.quantize(x, fp8.E4M3, out=qr))
+    out["cast_gbs"]["rows_e5m2"] = one / timed(lambda: fp8.quantize(x, fp8.E5M2, out=qr))
+    out["cast_gbs"]["transposed_e4m3"] = one / timed(lambda: fp8.quantize(x, fp8.E4M3, transpose=True, out=qt))
+    out["cast_gbs"]["transposed_dbias_e5m2"] = (one + R // 128 * C * 4 / 1e6) / timed(
+        lambda: fp8.quantize_dbias(x, fp8.E5M2, out_t=qt, dbias=db, workspace=ws))
+    out["cast_gbs"]["dual_e4m3"] = n * (2.0 + 2.0 * (1.0 + 4.0 / 128)) / 1e6 / timed(
+        lambda: fp8.quantize_dual(x, fp8.E4M3, out=qr, out_t=qt))
+    out["hbm_peak_gbs"] = peaks()[1]
+    out["frac_of_hbm"] = {k: v / out["hbm_peak_gbs"] for k, v in out["cast_gbs"].items()}
+    out["status"] = fp8.device_status()
+    print(json.dumps(out))
+
+
 def run_wgrad_tables(args):
     """The weight-gradient tables: the dense sweep (six (M, N) shapes x K in
     {4096, 8192}, fp32 out += A B^T) and the k-grouped MoE table (G experts,
@@ -702,6 +755,15 @@ def run_wgrad_tables(args):
         A, Bq = operand(M, tot), operand(N, tot)
         out = torch.zeros((G, M, N), device="cuda")
         grouped["g%d_m%d_n%d_tokens%d" % (G, M, N, tot)] = {
+            "k_sizes": ks, "tflops": 2.0 * M * N * tot / 1e9 / timed(lambda: fp8.grouped_wgrad(A, Bq, ks, out))}
+        del A, Bq, out
+    # a skewed split of 16384 tokens (60%, none, 25%, 15%) over 4 experts, the
+    # large expert first and last in turn: the host schedules groups longest first
+    for ks in ([9856, 0, 4096, 2432], [2432, 0, 4096, 9856]):
+        M, N, tot = 2048, 7168, sum(ks)
+        A, Bq = operand(M, tot), operand(N, tot)
+        out = torch.zeros((len(ks), M, N), device="cuda")
+        grouped["skewed_g4_m%d_n%d_tokens%d_%s" % (M, N, tot, "_".join(map(str, ks)))] = {
             "k_sizes": ks, "tflops": 2.0 * M * N * tot / 1e9 / timed(lambda: fp8.grouped_wgrad(A, Bq, ks, out))}
         del A, Bq, out
     print(json.dumps({"study": "wgrad_tables", "reps": reps, "dense_tflops": dense, "grouped": grouped,
@@ -901,6 +963,8 @@ def main():
         return run_mx_study(args)
     if args.study == "tensor":
         return run_tensor_study(args)
+    if args.study == "casts":
+        return run_cast_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libfp8ll.so")
 E4M3, E5M2 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_DGELU, EPI_DGELU_BGRAD = 0, 1, 2, 3, 4
 ACC_FULL, ACC_FAST = 0, 1
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE, ERR_SCRATCH = 0, -1, -2, -3, -4, -5, -6
 
 # every symbol include/fp8ll.h declares
 EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",

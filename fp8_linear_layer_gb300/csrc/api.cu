@@ -349,7 +349,7 @@ int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     p.out = out_bf16;
     p.aux = (epi == FP8LL_EPI_BIAS_GELU) ? aux_bf16 : nullptr;
     p.bias = bias_bf16;
-    return launch_gemm_fprop(maps, p, epi, acc_mode, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+    return launch_gemm_fprop(maps, p, epi, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }
@@ -394,7 +394,7 @@ int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
         p.z_tma = 1;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_gemm_dgrad(maps, p, epi, acc_mode, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
+    if (launch_gemm_dgrad(maps, p, epi, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
     if (epi == FP8LL_EPI_DGELU_BGRAD) {
         if (launch_bgrad_finalize(static_cast<const float*>(workspace), static_cast<int64_t>(p.num_m_tiles) * 4, N,
                                   bgrad, s, dev->num_sms) != 0)
@@ -463,7 +463,7 @@ int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const
     p.total_tiles = ng * p.tiles_per_group;
     p.out = out;
     p.accumulate = accumulate;
-    return launch_gemm_wgrad(maps, p, acc_mode, s, grid_for(p, dev)) == 0 ? FP8LL_OK : FP8LL_ERR_LAUNCH;
+    return launch_gemm_wgrad(maps, p, s, grid_for(p, dev)) == 0 ? FP8LL_OK : FP8LL_ERR_LAUNCH;
 }
 
 int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
@@ -527,8 +527,18 @@ int fp8_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t l
     const int64_t part_bytes = (rows / 128) * cols * 4;
     if (!workspace || !aligned16(workspace) || static_cast<int64_t>(workspace_bytes) < part_bytes)
         return FP8LL_ERR_WORKSPACE;
-    // the finalize reads the partials while it writes dbias
-    if (overlaps(dbias, cols * 4, workspace, part_bytes)) return FP8LL_ERR_INVALID_ARG;
+    // the cast kernel writes the partials while it reads x and writes the
+    // codes and scales, and the finalize reads them while it writes dbias
+    const int64_t x_bytes = ((rows - 1) * ldx + cols) * 2;
+    const int64_t qc_bytes = cols * rows, sc_bytes = ((rows / 128 - 1) * scale_ld_cols + cols) * 4;
+    if (overlaps(dbias, cols * 4, workspace, part_bytes) || overlaps(x_bf16, x_bytes, workspace, part_bytes) ||
+        overlaps(q_cols, qc_bytes, workspace, part_bytes) || overlaps(scale_cols, sc_bytes, workspace, part_bytes))
+        return FP8LL_ERR_INVALID_ARG;
+    if (q_rows) {
+        const int64_t qr_bytes = rows * cols, sr_bytes = ((cols / 128 - 1) * scale_ld_rows + rows) * 4;
+        if (overlaps(q_rows, qr_bytes, workspace, part_bytes) || overlaps(scale_rows, sr_bytes, workspace, part_bytes))
+            return FP8LL_ERR_INVALID_ARG;
+    }
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
     return launch_quantize_dbias(x_bf16, rows, cols, ldx, fmt, q_cols, scale_cols, scale_ld_cols, q_rows, scale_rows,
@@ -560,7 +570,12 @@ int fp8_mx_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_
     const int64_t part_bytes = (rows / 128) * cols * 4;
     if (!workspace || !aligned16(workspace) || static_cast<int64_t>(workspace_bytes) < part_bytes)
         return FP8LL_ERR_WORKSPACE;
-    if (overlaps(dbias, cols * 4, workspace, part_bytes)) return FP8LL_ERR_INVALID_ARG;
+    // as fp8_quantize_dbias: the partials may not overlap what the cast reads or writes
+    const int64_t x_bytes = ((rows - 1) * ldx + cols) * 2;
+    const int64_t sf_bytes = static_cast<int64_t>(fp8_mx_sf_bytes(cols, rows));
+    if (overlaps(dbias, cols * 4, workspace, part_bytes) || overlaps(x_bf16, x_bytes, workspace, part_bytes) ||
+        overlaps(q, cols * rows, workspace, part_bytes) || overlaps(sf, sf_bytes, workspace, part_bytes))
+        return FP8LL_ERR_INVALID_ARG;
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
     return launch_mx_quantize_dbias(x_bf16, rows, cols, ldx, fmt, q, sf, static_cast<float*>(workspace), dbias,
@@ -592,6 +607,7 @@ const char* fp8_status_string(int code) {
         case FP8LL_ERR_LAUNCH: return "CUDA launch or driver error";
         case FP8LL_ERR_TIMEOUT: return "kernel pipeline wait timed out";
         case FP8LL_ERR_WORKSPACE: return "workspace missing or too small";
+        case FP8LL_ERR_SCRATCH: return "built-in scratch array unavailable on this device";
         default: return "unknown status";
     }
 }

@@ -44,17 +44,11 @@ int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* 
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, int fast, cudaStream_t stream,
-                      int grid) {
+int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
     switch (epi) {
-        case kEpiDgelu:
-            return fast ? launch_gemm_impl<kEpiDgelu, true>(maps, p, stream, grid)
-                        : launch_gemm_impl<kEpiDgelu, false>(maps, p, stream, grid);
-        case kEpiDgeluBgrad:
-            return fast ? launch_gemm_impl<kEpiDgeluBgrad, true>(maps, p, stream, grid)
-                        : launch_gemm_impl<kEpiDgeluBgrad, false>(maps, p, stream, grid);
-        default:
-            return -1;
+        case kEpiDgelu: return launch_gemm_impl<kEpiDgelu>(maps, p, stream, grid);
+        case kEpiDgeluBgrad: return launch_gemm_impl<kEpiDgeluBgrad>(maps, p, stream, grid);
+        default: return -1;
     }
 }
 

@@ -463,7 +463,7 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
 
 // -------------------------------------------------------------------- kernel
 
-template <int EPI, bool FAST>
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -756,9 +756,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int EPI, bool FAST>
+template <int EPI>
 int launch_gemm_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid) {
-    auto kern = gemm_fp8_kernel<EPI, FAST>;
+    auto kern = gemm_fp8_kernel<EPI>;
     static unsigned long long configured = 0;  // one bit per device ordinal
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;

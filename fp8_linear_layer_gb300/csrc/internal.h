@@ -36,11 +36,11 @@ int launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, i
 int launch_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, cudaStream_t stream, int num_sms);
 
 // GEMM launchers, one per epilogue family (separate translation units).
-int launch_gemm_fprop(const TensorMaps& maps, const GemmParams& p, int epi, int fast, cudaStream_t stream,
-                      int grid);
-int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, int fast, cudaStream_t stream,
-                      int grid);
-int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, int fast, cudaStream_t stream, int grid);
+// The 1x128 GEMM has one promotion schedule: FP8LL_ACC_FAST is accepted by the
+// entry points and runs it (every K block meets its own scale pair).
+int launch_gemm_fprop(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
+int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
+int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid);
 int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_gemm_tensor(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* bgrad, cudaStream_t stream,

@@ -73,10 +73,13 @@ enum {
  * should use fast accumulation": DEFAULT = fast, HIGHEST = full).
  *   FULL: each 128-deep K block's fp32 partial product is promoted into the
  *         fp32 accumulator with its own scale pair as soon as it is ready.
- *   FAST: accepted on every GEMM; with one fp32 scale per row per 128-element
- *         block, every block's partial product must still meet its own scale
- *         pair, so FAST currently runs the FULL promotion (same results, same
- *         speed).  Results meet the FULL bound, inside the FAST one. */
+ *   FAST: accepted on every GEMM and runs the FULL promotion: results are
+ *         bit-identical to FULL, inside the FAST bound.  With one fp32 scale
+ *         per row per 128-element block, every block's partial product must
+ *         meet its own scale pair (applying one block's pair to a window of
+ *         blocks is off by the ratio of their scales), and promoting several
+ *         blocks in one batch needs more tensor-memory accumulators than the
+ *         512 columns hold at 256-column output tiles. */
 enum { FP8LL_ACC_FULL = 0, FP8LL_ACC_FAST = 1 };
 
 enum {
@@ -85,7 +88,8 @@ enum {
     FP8LL_ERR_UNSUPPORTED_DEVICE = -2, /* current device is not sm_103 */
     FP8LL_ERR_LAUNCH = -3,           /* a CUDA launch or driver call failed */
     FP8LL_ERR_TIMEOUT = -4,          /* a kernel pipeline wait ran out of time */
-    FP8LL_ERR_WORKSPACE = -5         /* workspace missing or too small */
+    FP8LL_ERR_WORKSPACE = -5,        /* workspace missing or too small */
+    FP8LL_ERR_SCRATCH = -6           /* fp8_gemm_dgrad_noalloc: the built-in scratch array could not be set up */
 };
 
 /* One fp8 operand: codes q[rows][ld_q] (row stride ld_q bytes, K contiguous)
@@ -166,7 +170,8 @@ int fp8_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
                    fp8ll_stream_t stream);
 
 /* Bytes of workspace fp8_gemm_dgrad needs for FP8LL_EPI_DGELU_BGRAD: one fp32
- * partial column sum per 128-row band of C, ceil(M/128) * N * 4. */
+ * partial column sum per 32-row band of C (each promotion warp of a 128-row
+ * tile writes its own band), 4 * ceil(M/128) * N * 4 bytes. */
 size_t fp8_workspace_size(int64_t M, int64_t N);
 
 /* Data-gradient GEMM with the GELU-derivative epilogue ("Replaced cublasLt
@@ -191,10 +196,18 @@ int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
  * this library.)  Same arguments and results as fp8_gemm_dgrad, minus the
  * workspace: the bias-gradient partials go to a fixed 16 MiB array inside the
  * library, held by every GPU that loads the library until the process exits.
- *   - Sizes with fp8_workspace_size(M, N) > 16 MiB (ceil(M/128) * 4 * N > 4 Mi
- *     partial sums) are refused with FP8LL_ERR_WORKSPACE before any launch.
+ *   - Arguments are checked exactly as fp8_gemm_dgrad checks them, and a bad
+ *     call gets the same code from both.  Sizes with fp8_workspace_size(M, N)
+ *     > 16 MiB (4 * ceil(M/128) * N > 4 Mi partial sums) are then refused
+ *     with FP8LL_ERR_WORKSPACE before any launch.
  *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current and keeps it.  Under lazy module loading (the CUDA
+ *     default) this first call is when the CUDA runtime loads the library
+ *     part that holds the array and reserves its 16 MiB: make it at start-up,
+ *     before the caller's own allocator takes the device's memory, and before
+ *     any stream capture.  If the runtime cannot provide the array, the call
+ *     returns FP8LL_ERR_SCRATCH.  The kept address does not survive
+ *     cudaDeviceReset (reload the library after a reset).
  *   - All calls share the one array: calls that overlap on the GPU (for
  *     example on two streams) race on it.  No clearing is needed between
  *     calls; every partial read is written by the same call first.
@@ -236,7 +249,8 @@ int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const
  * rows % 128 == 0, cols % 8 == 0, ldx >= cols, ldx % 8 == 0.  rows == 0 sets
  * dbias to zero.  workspace: >= (rows/128) * cols * 4 bytes, 16-byte aligned
  * (fp8_workspace_size(rows, cols) is enough), else FP8LL_ERR_WORKSPACE; it
- * holds per-128-row partial sums and may not overlap dbias.  The sums run in
+ * holds per-128-row partial sums and may overlap none of x, the codes, the
+ * scales or dbias (FP8LL_ERR_INVALID_ARG).  The sums run in
  * fp32 in a fixed order (each 128-row block, then the blocks): deterministic. */
 int fp8_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
                        float* scale_cols, int64_t scale_ld_cols, uint8_t* q_rows, float* scale_rows,
@@ -318,7 +332,7 @@ int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
  * for the MXFP8 recipe's transposed cast of the gradient).  Codes and scale
  * bytes are exactly fp8_mx_quantize's; rows % 128 == 0, cols % 8 == 0;
  * rows == 0 sets dbias to zero.  workspace: >= (rows/128) * cols * 4 bytes,
- * 16-byte aligned, not overlapping dbias.  The sums run in the same fixed order
+ * 16-byte aligned, overlapping none of x, q, sf or dbias.  The sums run in the same fixed order
  * as fp8_quantize_dbias's, so the two give the same bits for the same x. */
 int fp8_mx_quantize_dbias(const void* x_bf16, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q,
                           uint8_t* sf, float* dbias, void* workspace, size_t workspace_bytes, fp8ll_stream_t stream);

@@ -51,6 +51,7 @@ def test_status_strings(L):
     assert f.status_string(0) == "ok"
     assert "timed out" in f.status_string(-4)
     assert f.status_string(12345) == "unknown status"
+    assert "scratch" in f.status_string(f.binding.ERR_SCRATCH)
 
 
 def test_invalid_arguments_rejected_on_host(L):
@@ -93,6 +94,16 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.fp8_grouped_wgrad(0, 8, 8, ks0, ob, ob, fake, 1, 0, None) == E
     assert L.fp8_grouped_wgrad(1, 8, 8, ks0, ob, ob, fake, 2, 0, None) == E             # accumulate flag
     assert L.fp8_debug_starve_next_gemm(0) == E
+    # the no-allocation data gradient checks arguments exactly as fp8_gemm_dgrad does, so a bad
+    # call gets the same code from both even when M x N is beyond its built-in scratch
+    nz = L.fp8_gemm_dgrad_noalloc
+    assert nz(8, 8, 256, ob, oo, fake, 4, 0, fake, fake, None) == E                      # bad operand
+    assert nz(8, 8, 200, ob, ob, fake, 4, 0, fake, fake, None) == E                      # K % 128
+    big = ctypes.byref(f.binding.OperandStruct(0x10000, 0x20000, 256, 65536, 0, 0))  # scales for 65536 rows
+    assert nz(4096, 65536, 256, big, oo, fake, 4, 0, fake, fake, None) == E              # bad operand, large
+    assert nz(4096, 65536, 256, big, big, fake, 4, 0, fake, None, None) == E             # no bgrad, large
+    assert nz(4096, 65536, 256, big, big, fake, 4, 0, fake, fake, None) == f.binding.ERR_WORKSPACE
+    assert nz(8, 8, 256, ob, ob, fake, 9, 0, fake, fake, None) == E                      # epilogue
 
 
 def test_tensor_scaling_validation(L):
@@ -189,6 +200,14 @@ def test_quantize_dbias_validation(L):
     assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, vp(0x500000 + 64), ws, need, None) == E  # db in ws
     assert fn(x, 256, 0, 64, 1, q, s, 64, None, None, 0, db, ws, need, None) == f.binding.OK  # no columns
     assert fn(x, 256, 64, 64, 2, q, s, 64, None, None, 0, db, ws, need, None) == E  # format
+    # the partials may not overlap what the cast reads (x) or writes (codes, scales)
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, db, vp(0x100000 + 256 * 128 - 16), need, None) == E
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, db, vp(0x200000 + 64 * 256 - 16), need, None) == E
+    assert fn(x, 256, 64, 64, 1, q, s, 64, None, None, 0, db, vp(0x300000 - need + 16), need, None) == E
+    q2, s2 = vp(0x600000), vp(0x700000)  # with the row cast: its codes and scales too
+    assert fn(x, 256, 128, 128, 1, q, s, 128, q2, s2, 256, db, vp(0x600000 + 256 * 128 - 16), 2 * 128 * 4,
+              None) == E
+    assert fn(x, 256, 128, 128, 1, q, s, 128, q2, s2, 256, db, vp(0x700000 + 16), 2 * 128 * 4, None) == E
 
 
 def test_binding_checks_every_status_with_its_call_name():
@@ -217,4 +236,7 @@ def test_mx_quantize_dbias_validation(L):
     assert fn(x, 256, 64, 64, 1, q, sf, vp(0x400001), ws, need, None) == E
     assert fn(x, 256, 64, 64, 1, q, sf, db, ws, need - 4, None) == WS
     assert fn(x, 256, 64, 64, 1, q, sf, vp(0x500000 + 256), ws, need, None) == E  # db inside the partials
+    assert fn(x, 256, 64, 64, 1, q, sf, db, vp(0x100000 + 256 * 128 - 16), need, None) == E  # ws over x's end
+    assert fn(x, 256, 64, 64, 1, q, sf, db, vp(0x200000 + 64 * 256 - 16), need, None) == E  # ws over the codes
+    assert fn(x, 256, 64, 64, 1, q, sf, db, vp(0x300000 + 16), need, None) == E  # ws over the scale bytes
     assert fn(x, 256, 0, 64, 1, q, sf, db, ws, need, None) == f.binding.OK

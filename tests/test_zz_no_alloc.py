@@ -41,33 +41,39 @@ def test_noalloc_dgrad_matches_allocating_entry_point_twice(fp8):
     B = fp8.quantize(w.cuda(), E4M3)
     ref_dz, ref_bg = fp8.gemm_dgrad(A, B, z, fp8.EPI_DGELU_BGRAD)
     torch.cuda.synchronize()
-    # the tolerance the other dgrad tests use, from the oracle's sum |a b|
+    # the oracle's dZ (float64, before bf16 rounding) and its column sums, with
+    # the bound the other data-gradient tests use (from the oracle's sum |a b|)
     qa, sa = oracle.quantize(workloads.bits(dy), E5M2)
     qb, sb = oracle.quantize(workloads.bits(w), E4M3)
     acc, S = oracle.gemm(qa, sa, E5M2, qb, sb, E4M3)
+    dzo = oracle.dgrad_epilogue(acc, workloads.bits(z))
+    dbo = oracle.colsum(dzo)
     zf = bf16_to_f64(z)
     g = np.abs(oracle.dgelu(zf))
     ev = np.abs(acc) * dgelu_eval_bound(zf)
-    r = bf16_to_f64(ref_dz)
+    elem = g * FULL_C * S + ev
     for _ in range(2):  # the second call finds the first call's partials in the array
         out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         bg = torch.full((N,), float("nan"), device="cuda")
         assert call_noalloc(fp8, A, B, z, out, bg, M, N, K) == 0
         torch.cuda.synchronize()
         assert fp8.device_status() == 0
+        # the same kernels in the same order as fp8_gemm_dgrad: identical bits
+        assert torch.equal(out.view(torch.int16), ref_dz.view(torch.int16)), "dZ differs from fp8_gemm_dgrad"
+        assert torch.equal(bg.view(torch.int32), ref_bg.view(torch.int32)), "bgrad differs from fp8_gemm_dgrad"
         d = bf16_to_f64(out)
-        assert_within(d, r, g * FULL_C * S + ev + bf16_ulp(np.maximum(np.abs(d), np.abs(r))), "dZ")
+        assert_within(d, dzo, elem + bf16_ulp(np.maximum(np.abs(d), np.abs(dzo))), "dZ vs oracle")
         bb = bg.cpu().double().numpy()
-        rb = ref_bg.cpu().double().numpy()
-        assert_within(bb, rb, (g * FULL_C * S + ev).sum(0) + 40 * 2.0 ** -24 * np.abs(r).sum(0) + 1e-30, "bgrad")
+        assert_within(bb, dbo, elem.sum(0) + 40 * 2.0 ** -24 * np.abs(dzo).sum(0) + 1e-30, "bgrad vs oracle")
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(fp8):
     # ceil(M/128) * 4 * N fp32 partials must fit in 16 MiB; 4096 x 65536 needs 32 MiB
     M, N, K = 4096, 65536, 128
     assert fp8.workspace_size(M, N) > SCRATCH_BYTES
-    A = fp8.quantize(torch.zeros(128, K, dtype=torch.bfloat16, device="cuda"), E5M2)
-    B = fp8.quantize(torch.zeros(128, K, dtype=torch.bfloat16, device="cuda"), E4M3)
+    # operands of the full sizes (arguments are checked before the size is)
+    A = fp8.quantize(torch.zeros(M, K, dtype=torch.bfloat16, device="cuda"), E5M2)
+    B = fp8.quantize(torch.zeros(N, K, dtype=torch.bfloat16, device="cuda"), E4M3)
     z = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     bg = torch.zeros(4, device="cuda")
