@@ -35,7 +35,7 @@ SEED = 1002  # base seed of the training-step workload
 WORKLOAD = "linear_train_step_m8192_k4096_n14336_bias_gelu"
 METRIC = "FP8 GEMM TFLOPS (fprop/dgrad/wgrad) and % of GB300 dense-FP8 peak, 1 GPU"
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor-core ratio on this part
-KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "common.cuh", "gemm_params.h", "gemm_fprop.cu", "gemm_dgrad.cu",
+KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "common.cuh", "cast_rule.cuh", "gemm_params.h", "gemm_fprop.cu", "gemm_dgrad.cu",
                   "gemm_wgrad.cu")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fp8_kernel_m8192_k4096_n14336_traffic.md")
 
@@ -93,7 +93,8 @@ def parse_args():
     ap.add_argument("--m", type=int, default=M_TOK, help="tokens (default: the training-step workload)")
     ap.add_argument("--k", type=int, default=K_IN, help="in-features")
     ap.add_argument("--n", type=int, default=N_OUT, help="out-features")
-    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx", "tensor", "casts"],
+    ap.add_argument("--study", choices=["long_k", "kernels", "fp8_peak", "wgrad_tables", "mx", "tensor", "casts",
+                                        "input_grad"],
                     default=None,
                     help="long_k: forward GEMM M=N=16384 at long K with 1%% outlier rows, FULL vs FAST, "
                          "TFLOPS and max normalized error vs the oracle on sampled 256x256 tiles")
@@ -714,6 +715,60 @@ def run_cast_study(args):
     print(json.dumps(out))
 
 
+def run_input_grad_study(args):
+    """The training step with the layer's input gradient (dX = dZ W, a fourth
+    GEMM) where dZ's row cast for dX comes either from the transposed cast's
+    read of dZ (dz_rows="cast") or from the data-gradient GEMM's epilogue
+    (dz_rows="dgrad", fp8_gemm_dgrad_quant): CUDA events around --reps steps
+    after 3 warm-ups, the two plans alternated over 5 rounds; plus the two
+    launches that differ (the data-gradient GEMM with and without the cast,
+    the transposed cast of dZ with and without the row codes)."""
+    import torch
+    import fp8_linear_layer_gb300 as fp8
+    from fp8_linear_layer_gb300.linear import LinearTrainStep
+    m, k, n = args.m, args.k, args.n
+    reps = max(1, args.reps)
+    dev = torch.device("cuda")
+    X, W, b, dY = (t.to(dev) for t in inputs(dev, m, k, n))
+    steps = {mode: LinearTrainStep(m, k, n, dev, input_grad=True, dz_rows=mode) for mode in ("cast", "dgrad")}
+
+    def run(st):
+        for _, fn in st.launches(X, W, b, dY):
+            fn()
+        st.input_grad(W)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(reps):
+            fn()
+        e0.record()
+        e0.synchronize()
+        return s0.elapsed_time(e0) / reps
+
+    res = {"study": "input_grad", "reps": reps, "m": m, "k": k, "n": n, "step_ms": {"cast": [], "dgrad": []}}
+    for _ in range(5):
+        for mode, st in steps.items():
+            res["step_ms"][mode].append(timed(lambda: run(st)))
+    f4 = 4 * 2.0 * m * n * k
+    res["step_tflops_median"] = {mode: f4 / sorted(v)[len(v) // 2] / 1e9 for mode, v in res["step_ms"].items()}
+    st = steps["dgrad"]
+    f = 2.0 * m * n * k / 1e9
+    res["dgrad_tflops"] = {
+        "dgelu": f / timed(lambda: fp8.gemm_dgrad(st.dYq, st.Wq, st.Z, fp8.EPI_DGELU, out=st.dZ)),
+        "dgelu_quant": f / timed(lambda: fp8.gemm_dgrad_quant(st.dYq, st.Wq, st.Z, out=st.dZ, q_out=st.dZq))}
+    res["dz_cast_us"] = {
+        "transposed_dbias": 1e3 * timed(lambda: fp8.quantize_dbias(st.dZ, fp8.E5M2, out_t=st.dZTq, dbias=st.db,
+                                                                    workspace=st.ws)),
+        "transposed_dbias_and_rows": 1e3 * timed(lambda: fp8.quantize_dbias(st.dZ, fp8.E5M2, out_t=st.dZTq, out=st.dZq,
+                                                                             dbias=st.db, workspace=st.ws))}
+    res["status"] = fp8.device_status()
+    print(json.dumps(res))
+
+
 def run_wgrad_tables(args):
     """The weight-gradient tables: the dense sweep (six (M, N) shapes x K in
     {4096, 8192}, fp32 out += A B^T) and the k-grouped MoE table (G experts,
@@ -965,6 +1020,8 @@ def main():
         return run_tensor_study(args)
     if args.study == "casts":
         return run_cast_study(args)
+    if args.study == "input_grad":
+        return run_input_grad_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -10,7 +10,7 @@ step of one layer built from those calls (``linear``).
 """
 from .binding import (ACC_FAST, ACC_FULL, E4M3, E5M2, EPI_BIAS, EPI_BIAS_GELU, EPI_DGELU, EPI_DGELU_BGRAD,
                       EPI_NONE, EXPORTS, Fp8Error, Fp8Tensor, cast_f32, debug_starve_next_gemm, device_status,
-                      empty_fp8, gemm_dgrad, gemm_fprop, gemm_wgrad, grouped_wgrad, lib, quantize, quantize_dual,
+                      empty_fp8, gemm_dgrad, gemm_dgrad_quant, gemm_fprop, gemm_wgrad, grouped_wgrad, lib, quantize, quantize_dual,
                       scale_ld, status_string, workspace_size, Fp8MxTensor, empty_mx, mx_gemm_dgrad, mx_gemm_fprop,
                       mx_gemm_wgrad, mx_quantize, mx_sf_bytes, Fp8TensorScaled, amax_history_update,
                       empty_tensor_scaled, tensor_amax, tensor_gemm_dgrad, tensor_gemm_fprop, tensor_gemm_wgrad,
@@ -18,7 +18,7 @@ from .binding import (ACC_FAST, ACC_FULL, E4M3, E5M2, EPI_BIAS, EPI_BIAS_GELU, E
 
 __all__ = ["ACC_FAST", "ACC_FULL", "E4M3", "E5M2", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_DGELU", "EPI_DGELU_BGRAD",
            "EPI_NONE", "EXPORTS", "Fp8Error", "Fp8Tensor", "cast_f32", "debug_starve_next_gemm", "device_status",
-           "empty_fp8", "gemm_dgrad", "gemm_fprop", "gemm_wgrad", "grouped_wgrad", "lib", "quantize", "quantize_dual", "scale_ld",
+           "empty_fp8", "gemm_dgrad", "gemm_dgrad_quant", "gemm_fprop", "gemm_wgrad", "grouped_wgrad", "lib", "quantize", "quantize_dual", "scale_ld",
            "status_string", "workspace_size", "Fp8MxTensor", "empty_mx", "mx_gemm_dgrad", "mx_gemm_fprop",
            "mx_gemm_wgrad", "mx_quantize", "mx_sf_bytes", "Fp8TensorScaled", "amax_history_update",
            "empty_tensor_scaled", "tensor_amax", "tensor_gemm_dgrad", "tensor_gemm_fprop", "tensor_gemm_wgrad",

@@ -23,7 +23,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSP
 
 # every symbol include/fp8ll.h declares
 EXPORTS = ("fp8_scale_ld", "fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_workspace_size",
-           "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
+           "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc", "fp8_gemm_dgrad_quant", "fp8_gemm_wgrad", "fp8_grouped_wgrad", "fp8_get_device_status",
            "fp8_status_string", "fp8_debug_starve_next_gemm", "fp8_mx_sf_bytes", "fp8_mx_quantize",
            "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad", "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize",
            "fp8_amax_history_update", "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
@@ -74,6 +74,7 @@ def lib():
         L.fp8_workspace_size.restype = sz
         L.fp8_gemm_dgrad.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp, sz, vp]
         L.fp8_gemm_dgrad_noalloc.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp, vp, vp]
+        L.fp8_gemm_dgrad_quant.argtypes = [i64, i64, i64, op, op, vp, i32, vp, vp, vp, i64, vp]
         L.fp8_gemm_wgrad.argtypes = [i64, i64, i64, op, op, vp, i32, i32, vp]
         L.fp8_grouped_wgrad.argtypes = [i32, i64, i64, ctypes.POINTER(ctypes.c_int64), op, op, vp, i32, i32, vp]
         L.fp8_get_device_status.argtypes = [vp]
@@ -97,7 +98,8 @@ def lib():
         L.fp8_bgrad_from_operand.argtypes = [i64, i64, op, vp, i32, vp]
         L.fp8_quantize_dbias.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, i64, vp, vp, sz, vp]
         L.fp8_mx_quantize_dbias.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]
-        for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_dgrad_noalloc",
+        for name in ("fp8_quantize", "fp8_quantize_dual", "fp8_cast_f32", "fp8_gemm_fprop", "fp8_gemm_dgrad",
+                     "fp8_gemm_dgrad_noalloc", "fp8_gemm_dgrad_quant",
                      "fp8_gemm_wgrad", "fp8_mx_quantize", "fp8_mx_gemm_fprop", "fp8_mx_gemm_dgrad",
                      "fp8_mx_gemm_wgrad", "fp8_tensor_amax", "fp8_tensor_quantize", "fp8_amax_history_update",
                      "fp8_tensor_gemm_fprop", "fp8_tensor_gemm_dgrad", "fp8_tensor_gemm_wgrad",
@@ -234,6 +236,26 @@ def gemm_dgrad(A: Fp8Tensor, B: Fp8Tensor, aux: torch.Tensor, epi: int = EPI_DGE
     _check(lib().fp8_gemm_dgrad(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(aux), int(epi), int(acc),
                                 _ptr(out), _ptr(bgrad), _ptr(workspace), ws_bytes, _stream()), "fp8_gemm_dgrad")
     return out, bgrad
+
+
+def gemm_dgrad_quant(A: Fp8Tensor, B: Fp8Tensor, aux: torch.Tensor, acc: int = ACC_FULL,
+                     out: Optional[torch.Tensor] = None, q_out: Optional[Fp8Tensor] = None,
+                     K: Optional[int] = None) -> Tuple[torch.Tensor, Fp8Tensor]:
+    """dZ (bf16 [M][N]) = (A B^T) * gelu'(aux) and the e5m2 row cast of that
+    dZ (exactly quantize(dZ, E5M2)) from the same epilogue; N % 128 == 0.
+    Returns (dZ, Fp8Tensor of dZ)."""
+    M, N = A.rows, B.rows
+    K = A.k if K is None else K
+    dev = A.q.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if q_out is None:
+        q_out = empty_fp8(M, N, E5M2, dev)
+    oa, ob = A.operand(), B.operand()
+    _check(lib().fp8_gemm_dgrad_quant(M, N, K, ctypes.byref(oa), ctypes.byref(ob), _ptr(aux), int(acc), _ptr(out),
+                                      _ptr(q_out.q), _ptr(q_out.scale), q_out.scale.stride(0), _stream()),
+           "fp8_gemm_dgrad_quant")
+    return out, q_out
 
 
 def gemm_wgrad(A: Fp8Tensor, B: Fp8Tensor, out: torch.Tensor, accumulate: bool = True, acc: int = ACC_FULL,

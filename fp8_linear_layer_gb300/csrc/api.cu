@@ -262,6 +262,12 @@ int tensor_setup(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* 
 
 using namespace fp8ll;
 
+// true when [a, a + na) and [b, b + nb) share a byte
+static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+}
+
 extern "C" {
 
 int64_t fp8_scale_ld(int64_t rows) { return rows <= 0 ? 0 : (rows + 3) / 4 * 4; }
@@ -403,6 +409,45 @@ int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     return FP8LL_OK;
 }
 
+int fp8_gemm_dgrad_quant(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                         const void* aux_bf16, int acc_mode, void* out_bf16, uint8_t* q, float* scale,
+                         int64_t scale_ld, fp8ll_stream_t stream) {
+    if (!valid_mn(M, N) || K < 128 || K % 128 != 0 || K >= (1LL << 36) || N % 128 != 0) return FP8LL_ERR_INVALID_ARG;
+    if (acc_mode != FP8LL_ACC_FULL && acc_mode != FP8LL_ACC_FAST) return FP8LL_ERR_INVALID_ARG;
+    if (!valid_operand(A, M, K) || !valid_operand(B, N, K)) return FP8LL_ERR_INVALID_ARG;
+    if (!out_bf16 || !aligned16(out_bf16) || !aux_bf16 || !aligned16(aux_bf16)) return FP8LL_ERR_INVALID_ARG;
+    if (!q || !aligned16(q) || !scale || !aligned16(scale) || scale_ld < M || scale_ld % 4 != 0)
+        return FP8LL_ERR_INVALID_ARG;
+    // the codes and scales are written while dZ is written and Z is read
+    const int64_t q_bytes = M * N, s_bytes = ((N / 128 - 1) * scale_ld + M) * 4, z_bytes = M * N * 2;
+    if (overlaps(q, q_bytes, out_bf16, z_bytes) || overlaps(q, q_bytes, aux_bf16, z_bytes) ||
+        overlaps(scale, s_bytes, out_bf16, z_bytes) || overlaps(scale, s_bytes, aux_bf16, z_bytes) ||
+        overlaps(q, q_bytes, scale, s_bytes))
+        return FP8LL_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != FP8LL_OK) return rc;
+    TensorMaps maps;
+    if (!encode_operand(A, M, K, 128, &maps.a, &maps.sa) || !encode_operand(B, N, K, kTileN, &maps.b, &maps.sb))
+        return FP8LL_ERR_LAUNCH;
+    GemmParams p;
+    init_params(p, M, N, A, B, dev);
+    p.num_groups = 1;
+    p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
+    p.total_tiles = p.tiles_per_group;
+    p.out = out_bf16;
+    p.aux = const_cast<void*>(aux_bf16);
+    p.qout = q;
+    p.qscale = scale;
+    p.qsld = scale_ld;
+    std::memset(&maps.z, 0, sizeof(maps.z));
+    if (!encode_z(aux_bf16, M, N, &maps.z)) return FP8LL_ERR_LAUNCH;  // N % 128 == 0: rows 16-byte aligned
+    p.z_tma = 1;
+    return launch_gemm_dgrad(maps, p, kEpiDgeluQuant, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+               ? FP8LL_OK
+               : FP8LL_ERR_LAUNCH;
+}
+
 int fp8_grouped_wgrad(int G, int64_t M, int64_t N, const int64_t* k_sizes, const fp8ll_operand_t* A,
                       const fp8ll_operand_t* B, float* out, int accumulate, int acc_mode, fp8ll_stream_t stream) {
     if (G < 1 || G > kMaxGroups || !k_sizes) return FP8LL_ERR_INVALID_ARG;
@@ -471,12 +516,6 @@ int fp8_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, co
     if (K < 0) return FP8LL_ERR_INVALID_ARG;
     const int64_t ks[1] = {K};
     return fp8_grouped_wgrad(1, M, N, ks, A, B, out, accumulate, acc_mode, stream);
-}
-
-// true when [a, a + na) and [b, b + nb) share a byte
-static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
 }
 
 int fp8_bgrad_from_operand(int64_t rows, int64_t K, const fp8ll_operand_t* A, float* db, int accumulate,

@@ -48,6 +48,7 @@ int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, cuda
     switch (epi) {
         case kEpiDgelu: return launch_gemm_impl<kEpiDgelu>(maps, p, stream, grid);
         case kEpiDgeluBgrad: return launch_gemm_impl<kEpiDgeluBgrad>(maps, p, stream, grid);
+        case kEpiDgeluQuant: return launch_gemm_impl<kEpiDgeluQuant>(maps, p, stream, grid);
         default: return -1;
     }
 }

@@ -47,6 +47,7 @@
 #pragma once
 #include <cstdint>
 
+#include "cast_rule.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -98,7 +99,7 @@ static_assert(sizeof(SmemLayout) % 1024 == 0, "Z buffer alignment");
 
 template <int EPI>
 constexpr bool uses_z() {
-    return EPI == kEpiDgelu || EPI == kEpiDgeluBgrad;
+    return EPI == kEpiDgelu || EPI == kEpiDgeluBgrad || EPI == kEpiDgeluQuant;
 }
 template <int EPI>
 constexpr size_t smem_bytes() {
@@ -461,6 +462,86 @@ __device__ __forceinline__ void store_dgrad(const GemmParams& p, int row0, int c
     }
 }
 
+// dgrad with the row cast of its output: dZ = acc * gelu'(Z) -> bf16 out as
+// in store_dgrad, and the e5m2 codes and 1x128 scales of the stored bf16 dZ,
+// blocked along N, exactly as the row cast would produce them from that
+// output (the cast rule of cast_rule.cuh on the same bf16 values).  N % 128
+// == 0, so the thread's half of the tile is one 128-column block of each of
+// its four rows, and the block's 128 values sit with the four lanes of the
+// thread's quad (32 each): the block amax is the quad's maximum.  A lane holds
+// two codes of every 8-column chunk; two quad transposes give each lane the
+// 32 contiguous codes of chunks 4 (lane % 4) .. +3 for two 16-byte stores.
+template <bool ZSMEM>
+__device__ __forceinline__ void store_dgrad_quant(const GemmParams& p, int row0, int col0,
+                                                  const uint64_t (&acc)[4 * kChunks], int lane, const uint8_t* zrow) {
+    uint16_t* out = static_cast<uint16_t*>(p.out);
+    const uint16_t* zp = static_cast<const uint16_t*>(p.aux);
+    const int g8 = lane >> 2;
+    const int cq = lane & 3;
+    uint32_t w[4 * kChunks];  // bf16 pairs of dZ, w[4c + r]
+    float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        uint32_t zw[4];
+        if (ZSMEM)
+            load_z_smem(zrow, g8, c, zw);
+        else
+            load_z_group(p, zp, true, row0, col0, c, zw);
+        const int col = col0 + 8 * c;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float2 a = unpack_f32x2(acc[4 * c + r]);
+            const uint32_t v = pack_bf16x2(a.x * dgelu_tanh(bf16_lo(zw[r])), a.y * dgelu_tanh(bf16_hi(zw[r])));
+            w[4 * c + r] = v;
+            amax[r] = fmaxf(amax[r], fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
+            const int row = row0 + 8 * r;
+            if (row < p.M && col < p.N)
+                *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(row) * p.N + col) = v;
+        }
+    }
+    const int cb = col0 - 2 * cq;  // first column of the thread's 128-column block
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 1));
+        amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 2));
+        float inv, s;
+        block_scale<1>(amax[r], inv, s);
+        // codes of chunk 4g + e as 16-bit halves: lo = chunks 4g, 4g + 1; hi = 4g + 2, 4g + 3
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+            uint32_t h16[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t v = w[4 * (4 * gq + e) + r];
+                h16[e] = encode2<1>(bf16_lo(v), bf16_hi(v), inv);
+            }
+            lo[gq] = h16[0] | (h16[1] << 16);
+            hi[gq] = h16[2] | (h16[3] << 16);
+        }
+        // lane j receives group j's halves from every lane of the quad
+        quad_transpose(lo, cq);
+        quad_transpose(hi, cq);
+        const int row = row0 + 8 * r;
+        if (row < p.M && cb < p.N) {
+            // chunk 4 cq + e: bytes of lanes 0..3 in order (each lane two codes)
+            uint32_t o[8];
+            o[0] = __byte_perm(lo[0], lo[1], 0x5410);
+            o[1] = __byte_perm(lo[2], lo[3], 0x5410);
+            o[2] = __byte_perm(lo[0], lo[1], 0x7632);
+            o[3] = __byte_perm(lo[2], lo[3], 0x7632);
+            o[4] = __byte_perm(hi[0], hi[1], 0x5410);
+            o[5] = __byte_perm(hi[2], hi[3], 0x5410);
+            o[6] = __byte_perm(hi[0], hi[1], 0x7632);
+            o[7] = __byte_perm(hi[2], hi[3], 0x7632);
+            uint4* dst = reinterpret_cast<uint4*>(p.qout + static_cast<int64_t>(row) * p.N + cb + 32 * cq);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            if (cq == 0) p.qscale[static_cast<int64_t>(cb >> 7) * p.qsld + row] = s;
+        }
+    }
+}
+
 // -------------------------------------------------------------------- kernel
 
 template <int EPI>
@@ -736,12 +817,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = warp_all(mbar_wait(smem_addr(&sm.zfull), zph, budget));
                     if (!ok) break;
                     const uint8_t* zrow = zs + half * (kHalfN / kZBoxCols) * kZBoxBytes + (q * 32 + g8) * 128 + 4 * cq;
-                    store_dgrad<EPI == kEpiDgeluBgrad, true>(p, row0, col0, acc, band, lane, zrow);
+                    if (EPI == kEpiDgeluQuant)
+                        store_dgrad_quant<true>(p, row0, col0, acc, lane, zrow);
+                    else
+                        store_dgrad<EPI == kEpiDgeluBgrad, true>(p, row0, col0, acc, band, lane, zrow);
                     // read with ordinary loads, refilled by TMA: order before the release
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&sm.zempty));
                     zph ^= 1u;
+                } else if (EPI == kEpiDgeluQuant) {
+                    store_dgrad_quant<false>(p, row0, col0, acc, lane, nullptr);
                 } else {
                     store_dgrad<EPI == kEpiDgeluBgrad, false>(p, row0, col0, acc, band, lane, nullptr);
                 }

@@ -17,6 +17,7 @@ enum EpiKind : int {
     kEpiDgelu = 3,
     kEpiDgeluBgrad = 4,
     kEpiWgrad = 5,  // fp32 out (+)= C
+    kEpiDgeluQuant = 6,  // dgrad: dZ = C * gelu'(Z) -> bf16, plus its e5m2 row cast (codes + 1x128 scales)
 };
 
 // One schedulable group of output tiles: all tiles of a group share the same
@@ -50,6 +51,9 @@ struct GemmParams {
     int64_t sfb_groups;
     const float* tsa;     // per-tensor scaling: the one fp32 scale of A and of B
     const float* tsb;
+    uint8_t* qout;        // kEpiDgeluQuant: e5m2 codes of the bf16 dZ, [M][N]
+    float* qscale;        // kEpiDgeluQuant: their scales, [N/128][qsld]
+    int64_t qsld;
     GroupEntry groups[kMaxGroups];
 };
 

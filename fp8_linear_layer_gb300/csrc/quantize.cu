@@ -16,48 +16,19 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "cast_rule.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fp8ll {
 
-template <int FMT>
-struct Fp8Fmt;
-template <>
-struct Fp8Fmt<0> {
-    static constexpr float kMax = 448.0f;
-    __device__ static uint16_t cvt2(float lo, float hi) { return cvt_e4m3x2(lo, hi); }
-};
-template <>
-struct Fp8Fmt<1> {
-    static constexpr float kMax = 57344.0f;
-    __device__ static uint16_t cvt2(float lo, float hi) { return cvt_e5m2x2(lo, hi); }
-};
-
-template <int FMT>
-__device__ __forceinline__ void block_scale(float amax, float& inv, float& scale) {
-    inv = 1.0f;
-    scale = 1.0f;
-    if (amax > 0.0f) {
-        const float t = __fdiv_rn(Fp8Fmt<FMT>::kMax, amax);
-        if (t <= FLT_MAX) {
-            inv = t;
-            scale = __fdiv_rn(amax, Fp8Fmt<FMT>::kMax);
-        }
-    }
-}
-
 // 8 values -> 8 codes packed little-endian in a uint2
 template <int FMT>
 __device__ __forceinline__ uint2 encode8(const float (&f)[8], float inv) {
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float a = __fmul_rn(f[2 * i], inv);
-        const float b = __fmul_rn(f[2 * i + 1], inv);
-        w[i] = Fp8Fmt<FMT>::cvt2(a, b);
-    }
+    for (int i = 0; i < 4; ++i) w[i] = encode2<FMT>(f[2 * i], f[2 * i + 1], inv);
     return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 

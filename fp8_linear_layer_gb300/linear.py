@@ -33,7 +33,7 @@ from . import binding as B
 
 class LinearTrainStep:
     def __init__(self, m: int, k: int, n: int, device="cuda", acc_mode: int = B.ACC_FULL,
-                 input_grad: bool = False, bias_grad: str = "cast"):
+                 input_grad: bool = False, bias_grad: str = "cast", dz_rows: str = "cast"):
         """``bias_grad`` picks where db = sum(dZ, axis=0) comes from ("Replaced
         cublasLt calls with rocblas gemm + 6 manually crafted epilogues" takes
         it by reducing the stored gradient): "cast" (the default) sums the
@@ -41,13 +41,20 @@ class LinearTrainStep:
         read; "dgrad" sums the fp32 dZ in the data-gradient GEMM's epilogue,
         before its bf16 rounding; "operand" reduces the weight-gradient GEMM's
         fp8 operand dZ^T over the tokens (the BGRADB form).  With "cast" and
-        "operand" the data-gradient GEMM runs without its column sums."""
+        "operand" the data-gradient GEMM runs without its column sums.
+        ``dz_rows`` (with ``input_grad=True``) picks who casts dZ by rows for
+        the input gradient: "cast" (the default) writes them from the same
+        read as the transposed cast; "dgrad" has the data-gradient GEMM's
+        epilogue write them (``fp8_gemm_dgrad_quant``; not with
+        bias_grad="dgrad", whose epilogue sums the columns instead)."""
         assert m % 128 == 0 and k % 128 == 0
         assert not input_grad or n % 128 == 0, "the two-way casts of W and dZ need n % 128 == 0"
         assert bias_grad in ("dgrad", "cast", "operand")
+        assert dz_rows in ("cast", "dgrad") and not (dz_rows == "dgrad" and bias_grad == "dgrad")
         self.m, self.k, self.n = m, k, n
         self.acc_mode = acc_mode
         self.bias_grad = bias_grad
+        self.dz_rows = dz_rows
         self.with_input_grad = input_grad
         self.weight_cached = False
         dev = torch.device(device)
@@ -106,21 +113,29 @@ class LinearTrainStep:
         return plan
 
     def _backward_plan(self, X, dY):
-        if self.with_input_grad:
+        rows_in_cast = self.with_input_grad and self.dz_rows == "cast"
+        rows_in_dgrad = self.with_input_grad and self.dz_rows == "dgrad"
+        if rows_in_cast:
             cast_dz = ("quantize", lambda: B.quantize_dual(self.dZ, B.E5M2, out=self.dZq, out_t=self.dZTq))
         else:
             cast_dz = ("quantize", lambda: B.quantize(self.dZ, B.E5M2, transpose=True, out=self.dZTq))
+        if rows_in_dgrad:
+            dgrad = ("gemm", lambda: B.gemm_dgrad_quant(self.dYq, self.Wq, self.Z, self.acc_mode, out=self.dZ,
+                                                        q_out=self.dZq))
+        else:
+            dgrad = ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, self.acc_mode,
+                                                  out=self.dZ))
         plan = [("quantize", lambda: B.quantize(dY, B.E5M2, out=self.dYq))]
         if self.bias_grad == "cast":
-            dzq = self.dZq if self.with_input_grad else None
+            dzq = self.dZq if rows_in_cast else None
             plan += [
-                ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, self.acc_mode, out=self.dZ)),
+                dgrad,
                 ("quantize", lambda: B.quantize_dbias(self.dZ, B.E5M2, out_t=self.dZTq, out=dzq, dbias=self.db,
                                                       workspace=self.ws)),
             ]
         elif self.bias_grad == "operand":
             plan += [
-                ("gemm", lambda: B.gemm_dgrad(self.dYq, self.Wq, self.Z, B.EPI_DGELU, self.acc_mode, out=self.dZ)),
+                dgrad,
                 cast_dz,
                 # right after the cast, while much of dZ^T is still in L2
                 ("reduce", lambda: B.bgrad_from_operand(self.dZTq, out=self.db)),

@@ -12,6 +12,7 @@
  *   fp8_tensor_*        per-tensor scaling (current or delayed amax)
  *   fp8_gemm_fprop      C = A B^T with bias / tanh-GELU epilogues, bf16 out
  *   fp8_gemm_dgrad      C = A B^T times gelu'(Z), optional bias-gradient sums
+ *   fp8_gemm_dgrad_quant  the same, also casting its bf16 output (e5m2 rows)
  *   fp8_gemm_wgrad      fp32 out (+)= A B^T
  *   fp8_grouped_wgrad   per-group fp32 out_g (+)= A_g B_g^T, groups along K
  *   fp8_bgrad_from_operand  bias gradient as row sums of a 1x128-scaled operand
@@ -188,6 +189,22 @@ size_t fp8_workspace_size(int64_t M, int64_t N);
 int fp8_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
                    const void* aux_bf16, int epi, int acc_mode, void* out_bf16, float* bgrad, void* workspace,
                    size_t workspace_bytes, fp8ll_stream_t stream);
+
+/* The data-gradient GEMM that also casts its own output for the next GEMM:
+ * fp8_gemm_dgrad with FP8LL_EPI_DGELU (dZ = C * gelu'(Z), bf16 [M][N] in
+ * out_bf16) plus the e5m2 codes and 1x128 scales of that stored bf16 dZ,
+ * blocked along N -- exactly fp8_quantize(dZ, M, N, N, FP8LL_E5M2, 0, q,
+ * scale, scale_ld), which the input-gradient GEMM dX = dZ W consumes.
+ * "Weight gradient kernels for dense and MoE models" notes that separate cast
+ * launches around the GEMMs cost end-to-end time; here the cast rides on the
+ * epilogue that already holds dZ.
+ *   N % 128 == 0 (each 128-column block of a row lies in one output tile).
+ *   q: [M][N] codes, 16-byte aligned; scale: [N/128][scale_ld] fp32, 16-byte
+ *   aligned, scale_ld >= M, scale_ld % 4 == 0.  q and scale may overlap
+ *   neither each other nor dZ or Z.  Other arguments as fp8_gemm_dgrad. */
+int fp8_gemm_dgrad_quant(int64_t M, int64_t N, int64_t K, const fp8ll_operand_t* A, const fp8ll_operand_t* B,
+                         const void* aux_bf16, int acc_mode, void* out_bf16, uint8_t* q, float* scale,
+                         int64_t scale_ld, fp8ll_stream_t stream);
 
 /* fp8_gemm_dgrad for callers that cannot allocate device memory -- a runtime
  * whose allocator owns all device memory and forbids allocations after

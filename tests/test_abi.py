@@ -104,6 +104,16 @@ def test_invalid_arguments_rejected_on_host(L):
     assert nz(4096, 65536, 256, big, big, fake, 4, 0, fake, None, None) == E             # no bgrad, large
     assert nz(4096, 65536, 256, big, big, fake, 4, 0, fake, fake, None) == f.binding.ERR_WORKSPACE
     assert nz(8, 8, 256, ob, ob, fake, 9, 0, fake, fake, None) == E                      # epilogue
+    # the data gradient that casts its own output: N % 128, scale_ld, overlapping outputs
+    dq = L.fp8_gemm_dgrad_quant
+    op8 = ctypes.byref(f.binding.OperandStruct(0x10000, 0x20000, 256, 8, 1, 0))
+    wide = ctypes.byref(f.binding.OperandStruct(0x10000, 0x20000, 256, 256, 0, 0))
+    outp, auxp, qp, sp = vp(0x1000000), vp(0x2000000), vp(0x3000000), vp(0x4000000)
+    assert dq(8, 200, 256, op8, wide, auxp, 0, outp, qp, sp, 8, None) == E               # N % 128
+    assert dq(8, 256, 256, op8, wide, auxp, 0, outp, qp, sp, 4, None) == E               # scale_ld < M
+    assert dq(8, 256, 256, op8, wide, auxp, 0, outp, vp(0x1000000 + 64), sp, 8, None) == E   # q inside dZ
+    assert dq(8, 256, 256, op8, wide, auxp, 0, outp, qp, vp(0x2000000 + 16), 8, None) == E   # scales inside Z
+    assert dq(8, 256, 256, op8, wide, auxp, 3, outp, qp, sp, 8, None) == E               # accumulation mode
 
 
 def test_tensor_scaling_validation(L):

@@ -69,6 +69,19 @@ def test_gemm_outputs_stay_in_bounds(fp8, M, N, K):
     assert G.intact(), "grouped wgrad"
 
 
+@pytest.mark.parametrize("M,N,K", [(129, 384, 128), (300, 640, 256)])
+def test_dgrad_quant_outputs_stay_in_bounds(fp8, M, N, K):
+    # the data gradient that casts its own output: dZ, its codes and scales
+    x = workloads.normal_bf16((M, K), 702, "x").cuda()
+    w = workloads.normal_bf16((N, K), 702, "w", std=0.05).cuda()
+    z = workloads.normal_bf16((M, N), 702, "z").cuda()
+    X, W = fp8.quantize(x, E5M2), fp8.quantize(w, E4M3)
+    dZ = Guarded((M, N), torch.bfloat16)
+    Q, gq = guarded_fp8(fp8, M, N, E5M2)
+    fp8.gemm_dgrad_quant(X, W, z, out=dZ.view, q_out=Q)
+    assert dZ.intact() and all(g.intact() for g in gq), "dgrad with the row cast"
+
+
 def test_casts_stay_in_bounds(fp8):
     x = workloads.normal_bf16((384, 136), 702, "c").cuda()
     T, gt = guarded_fp8(fp8, 136, 384, E5M2)

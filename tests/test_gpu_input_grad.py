@@ -64,13 +64,23 @@ def test_train_step_with_two_way_casts_is_bit_identical(fp8):
     b = workloads.normal_bf16((n,), 73, "b", std=0.02).cuda()
     dY = workloads.normal_bf16((m, k), 73, "dy", std=1e-2).cuda()
     plain, fused = LinearTrainStep(m, k, n), LinearTrainStep(m, k, n, input_grad=True)
+    # and dZ's row codes for dX written by the data-gradient GEMM's epilogue instead
+    by_epilogue = LinearTrainStep(m, k, n, input_grad=True, dz_rows="dgrad")
+    operand = LinearTrainStep(m, k, n, input_grad=True, dz_rows="dgrad", bias_grad="operand")
     outs = []
-    for st in (plain, fused):
+    for st in (plain, fused, by_epilogue):
         st.step(X, W, b, dY)
         outs.append((st.Y.clone(), st.Z.clone(), st.dZ.clone(), st.db.clone(), st.dW.clone(),
                      st.input_grad(W).clone()))
     torch.cuda.synchronize()
-    for a, c in zip(*outs):
+    for o in outs[1:]:
+        for a, c in zip(outs[0], o):
+            assert torch.equal(a, c)
+    # the operand-reduced db differs (it sums the fp8 values); every other output agrees
+    operand.step(X, W, b, dY)
+    dx = operand.input_grad(W)
+    torch.cuda.synchronize()
+    for a, c in zip(outs[0][:3] + outs[0][4:], (operand.Y, operand.Z, operand.dZ, operand.dW, dx)):
         assert torch.equal(a, c)
 
 
