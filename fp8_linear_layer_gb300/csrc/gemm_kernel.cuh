@@ -131,8 +131,6 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
     nt = r / bm;
 }
 
-__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v) != 0; }
-
 // ------------------------------------------------------------------ stores
 //
 // After the promotion a thread holds the 16x256b TMEM fragment of its warp:
@@ -700,8 +698,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_tile(p, t, g, mt, nt);
             const int nkb = p.groups[g].nkb;
             for (int kb = 0; kb < nkb; ++kb) {
-                ok = warp_all(mbar_wait(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget));
-                if (ok) ok = warp_all(mbar_wait(smem_addr(&sm.full[s]), ph, budget));
+                ok = mbar_wait_warp(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget);
+                if (ok) ok = mbar_wait_warp(smem_addr(&sm.full[s]), ph, budget);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
@@ -761,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int kb = 0; kb < ge.nkb; ++kb) {
-                ok = warp_all(mbar_wait2(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget));
+                ok = mbar_wait2_warp(smem_addr(&sm.acc_full[ab]), aph, smem_addr(&sm.sfull[ss]), sph, budget);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tbuf = tq + static_cast<uint32_t>(ab * kBN);
@@ -782,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the block's partial sums are all in registers: hand the buffer back
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+                        mbar_arrive_lane0(smem_addr(&sm.acc_empty[ab]), lane);
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -798,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // TMA: order the reads before the release (cross-proxy hazard)
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&sm.sempty[ss]));
+                mbar_arrive_lane0(smem_addr(&sm.sempty[ss]), lane);
                 ring_advance<kNumAcc>(ab, aph);
                 ring_advance<kSStages>(ss, sph);
             }
@@ -814,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
                                                       : nullptr;
                 if (z_staged) {
-                    ok = warp_all(mbar_wait(smem_addr(&sm.zfull), zph, budget));
+                    ok = mbar_wait_warp(smem_addr(&sm.zfull), zph, budget);
                     if (!ok) break;
                     const uint8_t* zrow = zs + half * (kHalfN / kZBoxCols) * kZBoxBytes + (q * 32 + g8) * 128 + 4 * cq;
                     if (EPI == kEpiDgeluQuant)
@@ -824,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // read with ordinary loads, refilled by TMA: order before the release
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(&sm.zempty));
+                    mbar_arrive_lane0(smem_addr(&sm.zempty), lane);
                     zph ^= 1u;
                 } else if (EPI == kEpiDgeluQuant) {
                     store_dgrad_quant<false>(p, row0, col0, acc, lane, nullptr);

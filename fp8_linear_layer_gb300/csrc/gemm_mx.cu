@@ -177,12 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
             // the accumulator must have been read by the epilogue of the tile that used it last
-            ok = warp_all(mbar_wait(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget));
+            ok = mbar_wait_warp(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget);
             if (!ok) break;
             tc_fence_after();
             const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * kBN);
             for (int kb = 0; kb < nkb; ++kb) {
-                ok = warp_all(mbar_wait(smem_addr(&sm.full[s]), ph, budget));
+                ok = mbar_wait_warp(smem_addr(&sm.full[s]), ph, budget);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     prefetch_l2(zrow + pc1);
                 }
             }
-            ok = warp_all(mbar_wait(smem_addr(&sm.acc_full[ab]), aph, budget));
+            ok = mbar_wait_warp(smem_addr(&sm.acc_full[ab]), aph, budget);
             if (!ok) break;
             tc_fence_after();
             uint64_t acc[4 * kChunks];
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the tile's sums are in registers: the accumulator goes back to the MMA warp
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&sm.acc_empty[ab]));
+            mbar_arrive_lane0(smem_addr(&sm.acc_empty[ab]), lane);
             ring_advance<kAccBufs>(ab, aph);
             if (TENSOR) {
                 const float st = __fmul_rn(*p.tsa, *p.tsb);

@@ -34,6 +34,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
+// The same arrive issued by lane 0 of a converged warp as one predicated
+// instruction: no branch, so the warp does not split and reconverge around it.
+__device__ __forceinline__ void mbar_arrive_lane0(uint32_t bar, int lane) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+                 "r"(lane)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                  "r"(bytes)
@@ -89,6 +97,30 @@ __device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2
     if (!ok1) ok1 = mbar_wait(b1, p1, budget_ns);
     if (ok1 && !ok2) ok2 = mbar_wait(b2, p2, budget_ns);
     return ok1 && ok2;
+}
+
+// Warp-wide forms of the two waits above, for a converged warp: every lane
+// polls and the warp leaves together as soon as any lane has seen the phase
+// complete (a completed phase stays complete until the thread that owns the
+// barrier's next phase, which waits on this warp, moves it on), so the lanes
+// never split and need no vote afterwards.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(0xffffffffu, global_timer_ns() - t0 > budget_ns)) return false;
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait2_warp(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2,
+                                                uint64_t budget_ns) {
+    bool ok1, ok2;
+    mbar_try_wait2(b1, p1, b2, p2, ok1, ok2);
+    if (__any_sync(0xffffffffu, ok1 && ok2)) return true;
+    return mbar_wait_warp(b1, p1, budget_ns) && mbar_wait_warp(b2, p2, budget_ns);
 }
 
 // Orders this thread's earlier generic-proxy accesses to shared memory before
