@@ -489,7 +489,7 @@ def run_ours(args):
                        "l2": "working set ~1.3 GB per step >> 129 MB L2 (no flush needed)",
                        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak},
             "roofline": {"bound": "tensor", "kernel": {"block128": "gemm_fp8_kernel", "mx": "gemm_mx_kernel",
-                                                       "tensor": "gemm_mx_kernel<TENSOR>"}[args.recipe]
+                                                       "tensor": "gemm_tensor_kernel (CTA pairs)"}[args.recipe]
                          + " (fprop, dgrad, wgrad launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8ll.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm_fprop.cu", "gemm_dgrad.cu", "gemm_wgrad.cu", "gemm_mx.cu", "noalloc.cu", "bgrad_operand.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm_fprop.cu", "gemm_dgrad.cu", "gemm_wgrad.cu", "gemm_mx.cu", "gemm_tensor.cu", "noalloc.cu", "bgrad_operand.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -245,10 +245,15 @@ int tensor_setup(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_operand_t* 
     int rc = current_device(dev);
     if (rc != FP8LL_OK) return rc;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode_codes(A->q, A->ld_q, M, K, 128, &maps.a) || !encode_codes(B->q, B->ld_q, N, K, kTileN, &maps.b))
+    // CTA pairs: each CTA loads 128 rows of A and 128 of B's 256 tile rows
+    if (!encode_codes(A->q, A->ld_q, M, K, 128, &maps.a) ||
+        !encode_codes(B->q, B->ld_q, N, K, kTileN / 2, &maps.b))
         return FP8LL_ERR_LAUNCH;
     fp8ll_operand_t pa{A->q, A->scale, A->ld_q, 0, A->fmt, 0}, pb{B->q, B->scale, B->ld_q, 0, B->fmt, 0};
     init_params(p, M, N, &pa, &pb, *dev);  // the plain kind::f8f6f4 instruction descriptor
+    p.num_m_pairs = static_cast<int32_t>((M + 255) / 256);
+    p.tiles_per_group = p.num_m_pairs * p.num_n_tiles;
+    p.idesc = (p.idesc & ~(0x1Fu << 24)) | ((256u >> 4) << 24);  // the pair's MMA: M = 256
     p.num_groups = 1;
     p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
     p.total_tiles = p.tiles_per_group;
@@ -823,7 +828,7 @@ int fp8_tensor_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_op
     p.out = out_bf16;
     p.aux = (epi == FP8LL_EPI_BIAS_GELU) ? aux_bf16 : nullptr;
     p.bias = bias_bf16;
-    return launch_gemm_tensor(maps, p, epi, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+    return launch_gemm_tensor(maps, p, epi, reinterpret_cast<cudaStream_t>(stream)) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }
@@ -847,7 +852,7 @@ int fp8_tensor_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_op
     p.aux = const_cast<void*>(aux_bf16);
     p.workspace = static_cast<float*>(workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_gemm_tensor(maps, p, epi, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
+    if (launch_gemm_tensor(maps, p, epi, s) != 0) return FP8LL_ERR_LAUNCH;
     if (epi == FP8LL_EPI_DGELU_BGRAD &&
         launch_bgrad_finalize(static_cast<const float*>(workspace), static_cast<int64_t>(p.num_m_tiles) * 4, N, bgrad,
                               s, dev->num_sms) != 0)
@@ -865,7 +870,7 @@ int fp8_tensor_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_tensor_op
     if (rc != FP8LL_OK) return rc;
     p.out = out;
     p.accumulate = accumulate;
-    return launch_gemm_tensor(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+    return launch_gemm_tensor(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream)) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }

@@ -21,12 +21,8 @@
 //               warp, and stored through the same epilogue functions.
 // The scale atoms are the layout the MX cast writes (see quantize.cu).
 //
-// TENSOR = true is the per-tensor scaled GEMM ("FP8 GEMM for the fprop should
-// use fast accumulation": one scale per operand tensor): no scale atoms, plain
-// kind::f8f6f4 MMAs accumulate the raw fp8 products over the whole K range in
-// one of two TMEM accumulators (alternating per tile: without scale slots the
-// 512 columns hold two), and the epilogue multiplies the fp32 sums by
-// fl32(sA * sB) once -- no promotion inside the K loop.
+// The per-tensor scaled GEMM (one scale per operand, no scale atoms) runs on
+// CTA pairs in gemm_tensor.cu.
 #include "gemm_kernel.cuh"
 
 namespace fp8ll {
@@ -45,8 +41,8 @@ struct __align__(1024) MxSmem {
     uint8_t sfb[kMxStages][1024];
     uint64_t full[kMxStages];
     uint64_t empty[kMxStages];
-    uint64_t acc_full[2];  // one accumulator (MXFP8) or two (per-tensor)
-    uint64_t acc_empty[2];
+    uint64_t acc_full[1];
+    uint64_t acc_empty[1];
     uint64_t drain;
     uint32_t tmem_base;
 };
@@ -80,7 +76,7 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t adesc, uint64_t bdes
         : "memory");
 }
 
-template <int EPI, bool TENSOR>
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -90,19 +86,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t budget = p.budget_ns;
     const int nkb = p.groups[0].nkb;
-    // per-tensor: two 256-column accumulators, so a tile's MMAs do not wait for
-    // the epilogue to read the previous tile; MXFP8 needs columns 256.. for scales
-    constexpr int kAccBufs = TENSOR ? 2 : 1;
+    // one 256-column accumulator: columns 256.. hold the scale slots
+    constexpr int kAccBufs = 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMxStages; ++s) {
             mbar_init(smem_addr(&sm.full[s]), 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_addr(&sm.acc_full[b]), 1);
-            mbar_init(smem_addr(&sm.acc_empty[b]), kEpiWarps);
-        }
+        mbar_init(smem_addr(&sm.acc_full[0]), 1);
+        mbar_init(smem_addr(&sm.acc_empty[0]), kEpiWarps);
         mbar_init(smem_addr(&sm.drain), 1);
         fence_mbar_init();
     }
@@ -136,15 +129,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         const uint32_t fb = smem_addr(&sm.full[s]);
-                        mbar_arrive_expect_tx(fb, kBM * kBK + kBN * kBK + (TENSOR ? 0 : 512 + 1024));
+                        mbar_arrive_expect_tx(fb, kBM * kBK + kBN * kBK + 512 + 1024);
                         tma_load_2d(smem_addr(sm.a[s]), &maps.a, fb, kb * kBK, m0);
                         tma_load_2d(smem_addr(sm.b[s]), &maps.b, fb, kb * kBK, n0);
-                        if (!TENSOR) {
-                            bulk_load(smem_addr(sm.sfa[s]),
-                                      p.sfa + (static_cast<int64_t>(kb) * p.sfa_groups + mt) * 512, 512, fb);
-                            bulk_load(smem_addr(sm.sfb[s]),
-                                      p.sfb + (static_cast<int64_t>(kb) * p.sfb_groups + 2 * nt) * 512, 1024, fb);
-                        }
+                        bulk_load(smem_addr(sm.sfa[s]), p.sfa + (static_cast<int64_t>(kb) * p.sfa_groups + mt) * 512,
+                                  512, fb);
+                        bulk_load(smem_addr(sm.sfb[s]),
+                                  p.sfb + (static_cast<int64_t>(kb) * p.sfb_groups + 2 * nt) * 512, 1024, fb);
                         ++n_issued;
                         ring_advance<kMxStages>(s, ph);
                     }
@@ -188,23 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint64_t adesc = smem_desc_k_sw128(smem_addr(sm.a[s]));
                     const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sm.b[s]));
-                    if (TENSOR) {
+                    const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
+                    sf_copy(tsf, smem_addr(sm.sfa[s]));
+                    sf_copy(tsf + 4, smem_addr(sm.sfb[s]));
+                    sf_copy(tsf + 8, smem_addr(sm.sfb[s] + 512));
 #pragma unroll
-                        for (int k = 0; k < kBK / 32; ++k)
-                            mma_f8f6f4(dacc, adesc + 2u * k, bdesc + 2u * k, p.idesc,
-                                       (kb > 0 || k > 0) ? 1u : 0u);
-                    } else {
-                        const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
-                        sf_copy(tsf, smem_addr(sm.sfa[s]));
-                        sf_copy(tsf + 4, smem_addr(sm.sfb[s]));
-                        sf_copy(tsf + 8, smem_addr(sm.sfb[s] + 512));
-#pragma unroll
-                        for (int k = 0; k < kBK / 32; ++k) {
-                            const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 4) |
-                                                   (static_cast<uint32_t>(k) << 29);
-                            mma_mx(dacc, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
-                                   (kb > 0 || k > 0) ? 1u : 0u);
-                        }
+                    for (int k = 0; k < kBK / 32; ++k) {
+                        const uint32_t idesc =
+                            p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+                        mma_mx(dacc, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
+                               (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(smem_addr(&sm.empty[s]));
                     if (kb == nkb - 1) mma_commit(smem_addr(&sm.acc_full[ab]));
@@ -270,12 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             mbar_arrive_lane0(smem_addr(&sm.acc_empty[ab]), lane);
             ring_advance<kAccBufs>(ab, aph);
-            if (TENSOR) {
-                const float st = __fmul_rn(*p.tsa, *p.tsb);
-                const uint64_t st2 = pack_f32x2(st, st);
-#pragma unroll
-                for (int j = 0; j < 4 * kChunks; ++j) acc[j] = mul_f32x2(acc[j], st2);
-            }
             const int row0 = m0 + q * 32 + g8;
             const int col0 = n0 + half * kHalfN + 2 * cq;
             if (EPI == kEpiWgrad) {
@@ -297,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kMxTmemCols);
 }
 
-template <int EPI, bool TENSOR>
+template <int EPI>
 int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid) {
-    auto kern = gemm_mx_kernel<EPI, TENSOR>;
+    auto kern = gemm_mx_kernel<EPI>;
     static unsigned long long configured = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
@@ -315,25 +293,16 @@ int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t str
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-template <bool TENSOR>
-int launch_family(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
+int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
     switch (epi) {
-        case kEpiNone: return launch_mx_impl<kEpiNone, TENSOR>(maps, p, stream, grid);
-        case kEpiBias: return launch_mx_impl<kEpiBias, TENSOR>(maps, p, stream, grid);
-        case kEpiBiasGelu: return launch_mx_impl<kEpiBiasGelu, TENSOR>(maps, p, stream, grid);
-        case kEpiDgelu: return launch_mx_impl<kEpiDgelu, TENSOR>(maps, p, stream, grid);
-        case kEpiDgeluBgrad: return launch_mx_impl<kEpiDgeluBgrad, TENSOR>(maps, p, stream, grid);
-        case kEpiWgrad: return launch_mx_impl<kEpiWgrad, TENSOR>(maps, p, stream, grid);
+        case kEpiNone: return launch_mx_impl<kEpiNone>(maps, p, stream, grid);
+        case kEpiBias: return launch_mx_impl<kEpiBias>(maps, p, stream, grid);
+        case kEpiBiasGelu: return launch_mx_impl<kEpiBiasGelu>(maps, p, stream, grid);
+        case kEpiDgelu: return launch_mx_impl<kEpiDgelu>(maps, p, stream, grid);
+        case kEpiDgeluBgrad: return launch_mx_impl<kEpiDgeluBgrad>(maps, p, stream, grid);
+        case kEpiWgrad: return launch_mx_impl<kEpiWgrad>(maps, p, stream, grid);
         default: return -3;
     }
-}
-
-int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
-    return launch_family<false>(maps, p, epi, stream, grid);
-}
-
-int launch_gemm_tensor(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
-    return launch_family<true>(maps, p, epi, stream, grid);
 }
 
 }  // namespace fp8ll
