@@ -31,20 +31,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // approximate fp32 divide (2 ulp): the results are rounded to bf16, whose
 // half-ulp is 2e-3 relative, so the evaluation error stays far below the
 // output's own rounding.
-__device__ __forceinline__ float gelu_tanh(float z) {
-    const float c2 = 1.5957691216057308f;  // 2 sqrt(2/pi)
-    const float x = fminf(fmaxf(c2 * (z + 0.044715f * z * z * z), -80.0f), 80.0f);
-    return __fdividef(z, 1.0f + __expf(-x));
+// Both take a pair of values (the two columns a thread holds of each
+// 8-column chunk): the polynomial parts run as packed fp32x2 operations (one
+// instruction for both values, each rounded as the scalar operation would be),
+// the exponential and the division per value.  With
+//   x = clamp(2 sqrt(2/pi) z (1 + 0.044715 z^2), +-80)
+//   gelu(z)  = z / (1 + e^-x)
+//   gelu'(z) = sp + 2 sqrt(2/pi) z (1 + 3 * 0.044715 z^2) sp sm,  sp = s(x), sm = e^-x sp.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ float2 f32x2_split(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
-__device__ __forceinline__ float dgelu_tanh(float z) {
-    const float c = 0.7978845608028654f;  // sqrt(2/pi)
-    const float z2 = z * z;
-    const float x = fminf(fmaxf(2.0f * c * (z + 0.044715f * z2 * z), -80.0f), 80.0f);
-    const float e = __expf(-x);
-    const float sp = __fdividef(1.0f, 1.0f + e);  // s(2u)
-    const float sm = e * sp;                      // s(-2u)
-    return sp + 2.0f * z * c * (1.0f + 3.0f * 0.044715f * z2) * sp * sm;
+// 2 sqrt(2/pi) z (1 + 0.044715 z^2) for both values, and z^2
+__device__ __forceinline__ uint64_t gelu_arg2(uint64_t z, uint64_t& z2) {
+    const uint64_t c2 = f32x2(1.5957691216057308f, 1.5957691216057308f);  // 2 sqrt(2/pi)
+    z2 = mul2(z, z);
+    return mul2(c2, mul2(z, fma2(z2, f32x2(0.044715f, 0.044715f), f32x2(1.0f, 1.0f))));
+}
+
+__device__ __forceinline__ float2 gelu_tanh2(float z0, float z1) {
+    uint64_t z2;
+    const float2 x = f32x2_split(gelu_arg2(f32x2(z0, z1), z2));
+    const float x0 = fminf(fmaxf(x.x, -80.0f), 80.0f), x1 = fminf(fmaxf(x.y, -80.0f), 80.0f);
+    return make_float2(__fdividef(z0, 1.0f + __expf(-x0)), __fdividef(z1, 1.0f + __expf(-x1)));
+}
+
+__device__ __forceinline__ float2 dgelu_tanh2(float z0, float z1) {
+    const uint64_t z = f32x2(z0, z1);
+    uint64_t z2;
+    const float2 x = f32x2_split(gelu_arg2(z, z2));
+    const float x0 = fminf(fmaxf(x.x, -80.0f), 80.0f), x1 = fminf(fmaxf(x.y, -80.0f), 80.0f);
+    const float e0 = __expf(-x0), e1 = __expf(-x1);
+    const uint64_t sp = f32x2(__fdividef(1.0f, 1.0f + e0), __fdividef(1.0f, 1.0f + e1));  // s(x)
+    const uint64_t sm = mul2(f32x2(e0, e1), sp);                                          // s(-x)
+    const uint64_t c2 = f32x2(1.5957691216057308f, 1.5957691216057308f);
+    const uint64_t v = mul2(mul2(c2, z), fma2(z2, f32x2(3.0f * 0.044715f, 3.0f * 0.044715f), f32x2(1.0f, 1.0f)));
+    return f32x2_split(fma2(mul2(v, sp), sm, sp));
 }
 
 // Hint that a global cache line will be read soon: fetched into L2 ahead of use.
