@@ -318,7 +318,7 @@ int fp8_quantize_dual(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld
     int rc = current_device(&dev);
     if (rc != FP8LL_OK) return rc;
     return launch_quantize_dual(x_bf16, rows, cols, ldx, fmt, q_rows, scale_rows, scale_ld_rows, q_cols, scale_cols,
-                                scale_ld_cols, reinterpret_cast<cudaStream_t>(stream)) == 0
+                                scale_ld_cols, reinterpret_cast<cudaStream_t>(stream), dev->num_sms) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }

@@ -12,7 +12,7 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
                     float* scale, int64_t sld, cudaStream_t stream, int num_sms);
 int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
                          float* scale_rows, int64_t sld_rows, uint8_t* q_cols, float* scale_cols, int64_t sld_cols,
-                         cudaStream_t stream);
+                         cudaStream_t stream, int num_sms);
 // transposed cast (and, with q_rows, the row cast too) of x plus db = column sums of x:
 // partials [rows/128][cols] in dpart, then the fixed-order finalize into dbias
 int launch_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,

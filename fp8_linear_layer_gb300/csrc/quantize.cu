@@ -107,11 +107,24 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 }
 
 // --------------------------------------------------------------- transposed
-// One CTA owns a 128-row x 128-column tile of x.  Blocks run down columns:
-// output row c of q (= input column c) gets 128 contiguous codes per block.
-// The tile is staged in shared memory as 64 words per row (bf16 pairs), with
-// each 32-row band rotated by 8 words so that the column-wise reads of the
-// four 32-row parts hit 32 distinct banks.
+// Blocks run down columns: output row c of q (= input column c) gets 128
+// contiguous codes per 128-row block.  A CTA casts 128-row x 128-column tiles
+// of x staged in shared memory as 64 words per row (bf16 pairs), each 32-row
+// band rotated by 8 words so that the column-wise reads of the four 32-row
+// parts hit 32 distinct banks.  Two kernels stage the tiles:
+//   quantize_cols_kernel       one tile per CTA, four CTAs per SM: each thread
+//                              loads its eight 16-byte pieces into registers,
+//                              so the row-blocked cast (ROWS) and the tensor's
+//                              amax (TENSOR) are taken from the loaded values.
+//   quantize_cols_pipe_kernel  persistent, three CTAs per SM, two staged
+//                              tiles: while a CTA casts one tile the next one
+//                              streams in by cp.async; for the casts that only
+//                              write the column-blocked codes (plain and with
+//                              the bias-gradient sums), where it measured
+//                              faster (5608 -> 5750 and 4579 -> 5515 GB/s at
+//                              32768 x 8192).  Reading the staged tile back for
+//                              the row codes made the two-way cast slower
+//                              (5078 -> 4561), hence the first kernel there.
 //
 // With ROWS the CTA also writes the row-blocked cast of its tile (128 columns
 // = one block per row; codes qr [rows][cols], scales sr [cols/128][sldr]):
@@ -131,9 +144,85 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // from the high-precision values before the fp8 rounding).  The amax pass adds
 // each thread's 32 values of a column in row order, the quad combines its four
 // parts with the amax pass's shuffles, and one lane writes the tile's partial
-// sum to dpart[blockIdx.y][c]; a finalize adds the row blocks in a fixed order.
-// Three CTAs per SM for the plain transposed cast (64 registers for four
-// spilled; three measured 7% faster), four for the two-way cast (faster there).
+// sum to dpart[row block][c]; a finalize adds the row blocks in a fixed order.
+
+// The column-blocked cast of one staged tile (rows r0.., columns c0.., row
+// block rb) for the persistent kernel: thread t handles column pair t / 4 and
+// 32-row part t % 4.  Two passes over the staged tile (amax, then encode)
+// instead of holding 64 values in registers.  quantize_cols_kernel below does
+// the same arithmetic inline (as a shared function it measured 2-6% slower
+// there).
+template <int FMT, bool TENSOR, bool DBIAS>
+__device__ __forceinline__ void cast_tile_cols(const uint32_t (*tile)[64], int64_t rows, int64_t cols, int64_t r0,
+                                               int64_t c0, int64_t rb, uint8_t* __restrict__ q,
+                                               float* __restrict__ scale, int64_t sld, float inv_t, float s_t,
+                                               float* __restrict__ dpart) {
+    const int cp = threadIdx.x >> 2;  // column pair 0..63
+    const int p = threadIdx.x & 3;    // 32-row part
+    const int64_t c = c0 + 2 * cp;
+    float inv_lo = inv_t, s_lo = s_t, inv_hi = inv_t, s_hi = s_t;
+    if (!TENSOR) {
+        float amax_lo = 0.0f, amax_hi = 0.0f;
+        float sum_lo = 0.0f, sum_hi = 0.0f;  // DBIAS
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
+            amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
+            amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
+            if (DBIAS) {
+                sum_lo = __fadd_rn(sum_lo, bf16_lo(w));
+                sum_hi = __fadd_rn(sum_hi, bf16_hi(w));
+            }
+        }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
+            amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
+            if (DBIAS) {
+                // a + b on one lane, b + a on its partner: the same bits on all four
+                sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, off));
+                sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, off));
+            }
+        }
+        block_scale<FMT>(amax_lo, inv_lo, s_lo);
+        block_scale<FMT>(amax_hi, inv_hi, s_hi);
+        if (DBIAS && p == 0 && c < cols) {
+            // cols is even: c + 1 < cols too
+            dpart[rb * cols + c] = sum_lo;
+            dpart[rb * cols + c + 1] = sum_hi;
+        }
+    }
+    if (c < cols) {
+        uint32_t wl[8], wh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t lo16[2], hi16[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t w0 = tile[32 * p + 4 * i + 2 * j][(cp + 8 * p) & 63];
+                const uint32_t w1 = tile[32 * p + 4 * i + 2 * j + 1][(cp + 8 * p) & 63];
+                lo16[j] = Fp8Fmt<FMT>::cvt2(__fmul_rn(bf16_lo(w0), inv_lo), __fmul_rn(bf16_lo(w1), inv_lo));
+                hi16[j] = Fp8Fmt<FMT>::cvt2(__fmul_rn(bf16_hi(w0), inv_hi), __fmul_rn(bf16_hi(w1), inv_hi));
+            }
+            wl[i] = lo16[0] | (lo16[1] << 16);
+            wh[i] = hi16[0] | (hi16[1] << 16);
+        }
+        uint4* dl = reinterpret_cast<uint4*>(q + c * rows + r0 + 32 * p);
+        uint4* dh = reinterpret_cast<uint4*>(q + (c + 1) * rows + r0 + 32 * p);
+        dl[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+        dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+        if (!TENSOR && p == 0) {
+            scale[rb * sld + c] = s_lo;
+            scale[rb * sld + c + 1] = s_hi;
+        }
+    }
+}
+
+// place of word 4 ch (16-byte piece ch, 0..15) of tile row rr in the stage
+__device__ __forceinline__ int staged_word(int rr, int ch) { return (ch * 4 + 8 * (rr >> 5)) & 63; }
+
 template <int FMT, bool ROWS, bool TENSOR, bool DBIAS = false>
 __global__ void __launch_bounds__(256, ROWS ? 4 : 3) quantize_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
@@ -269,6 +358,91 @@ __global__ void __launch_bounds__(256, ROWS ? 4 : 3) quantize_cols_kernel(const 
             scale[static_cast<int64_t>(blockIdx.y) * sld + c] = s_lo;
             scale[static_cast<int64_t>(blockIdx.y) * sld + c + 1] = s_hi;
         }
+    }
+}
+
+constexpr int kPipeCtas = 3;                                    // CTAs per SM
+constexpr size_t kPipeSmem = 2 * 128 * 64 * sizeof(uint32_t);  // two staged tiles
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    // src_bytes 0 fills the 16 bytes with zeros and reads nothing
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <int FMT, bool DBIAS>
+__global__ void __launch_bounds__(256, kPipeCtas) quantize_cols_pipe_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
+    float* __restrict__ scale, int64_t sld, float* __restrict__ dpart) {
+    extern __shared__ __align__(16) uint32_t stage[];  // [2][128][64]
+    const int64_t ncb = (cols + 127) / 128;
+    const int64_t ntiles = (rows / 128) * ncb;
+
+    // thread t, copy it: row (t + 256 it) / 16 of the tile, columns
+    // 8 ((t + 256 it) % 16) .. +7, to its rotated place in the stage
+    auto fetch = [&](int64_t t, int buf) {
+        const int64_t rb = t / ncb;
+        const int64_t r0 = rb * 128, c0 = (t - rb * ncb) * 128;
+        const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(stage)) + buf * (128 * 64 * 4);
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int i = threadIdx.x + it * 256;
+            const int rr = i >> 4;
+            const int ch = i & 15;
+            const int64_t c = c0 + ch * 8;
+            const bool in = c < cols;
+            cp_async16(base + (rr * 64 + staged_word(rr, ch)) * 4, x + (r0 + rr) * ldx + (in ? c : 0),
+                       in ? 16u : 0u);
+        }
+    };
+
+    int64_t t = blockIdx.x;
+    if (t < ntiles) fetch(t, 0);
+    cp_async_commit();
+    for (int k = 0; t < ntiles; ++k, t += gridDim.x) {
+        const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(stage + (k & 1) * 128 * 64);
+        // every thread is done with the previous tile: its stage is refilled now
+        __syncthreads();
+        if (t + gridDim.x < ntiles) fetch(t + gridDim.x, (k + 1) & 1);
+        cp_async_commit();
+        cp_async_wait_all_but_one();  // this thread's copies of this tile have landed
+        __syncthreads();              // ... and every thread's
+        const int64_t rb = t / ncb;
+        cast_tile_cols<FMT, false, DBIAS>(tile, rows, cols, rb * 128, (t - rb * ncb) * 128, rb, q, scale, sld, 1.0f,
+                                          1.0f, dpart);
+    }
+}
+
+// The column-blocked cast (with ROWS also the row-blocked one): the one-tile
+// kernel where rows or a per-tensor scale are involved, the persistent one
+// otherwise.
+template <int FMT, bool ROWS, bool TENSOR, bool DBIAS>
+int launch_cols(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q, float* scale, int64_t sld,
+                uint8_t* qr, float* sr, int64_t sldr, const float* amax_in, unsigned* amax_out, float* dpart,
+                cudaStream_t stream, int num_sms) {
+    if constexpr (ROWS || TENSOR) {
+        dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+        quantize_cols_kernel<FMT, ROWS, TENSOR, DBIAS><<<grid, 256, 0, stream>>>(x, rows, cols, ldx, q, scale, sld, qr,
+                                                                                sr, sldr, amax_in, amax_out, dpart);
+        return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    } else {
+        auto kern = quantize_cols_pipe_kernel<FMT, DBIAS>;
+        static unsigned long long configured = 0;  // one bit per device ordinal
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
+        if (!(configured & (1ull << dev))) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPipeSmem)) !=
+                cudaSuccess)
+                return -3;
+            configured |= 1ull << dev;
+        }
+        const int64_t ntiles = (rows / 128) * ((cols + 127) / 128);
+        if (ntiles == 0) return 0;
+        const int64_t cap = static_cast<int64_t>(num_sms) * kPipeCtas;
+        const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
+        kern<<<grid, 256, kPipeSmem, stream>>>(x, rows, cols, ldx, q, scale, sld, dpart);
+        return cudaGetLastError() == cudaSuccess ? 0 : -3;
     }
 }
 
@@ -570,54 +744,42 @@ int launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, int 
                 quantize_rows_kernel<1, U, false><<<g, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld);
         }
     } else {
-        dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
-        if (fmt == 0)
-            quantize_cols_kernel<0, false, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld,
-                                                                             nullptr, nullptr, 0, nullptr, nullptr);
-        else
-            quantize_cols_kernel<1, false, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q, scale, sld,
-                                                                             nullptr, nullptr, 0, nullptr, nullptr);
+        return fmt == 0 ? launch_cols<0, false, false, false>(xb, rows, cols, ldx, q, scale, sld, nullptr, nullptr, 0,
+                                                              nullptr, nullptr, nullptr, stream, num_sms)
+                        : launch_cols<1, false, false, false>(xb, rows, cols, ldx, q, scale, sld, nullptr, nullptr, 0,
+                                                              nullptr, nullptr, nullptr, stream, num_sms);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 int launch_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_rows,
                          float* scale_rows, int64_t sld_rows, uint8_t* q_cols, float* scale_cols, int64_t sld_cols,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int num_sms) {
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
-    if (fmt == 0)
-        quantize_cols_kernel<0, true, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols,
-                                                                        sld_cols, q_rows, scale_rows, sld_rows,
-                                                                        nullptr, nullptr);
-    else
-        quantize_cols_kernel<1, true, false><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale_cols,
-                                                                        sld_cols, q_rows, scale_rows, sld_rows,
-                                                                        nullptr, nullptr);
-    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    return fmt == 0 ? launch_cols<0, true, false, false>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows,
+                                                         scale_rows, sld_rows, nullptr, nullptr, nullptr, stream,
+                                                         num_sms)
+                    : launch_cols<1, true, false, false>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows,
+                                                         scale_rows, sld_rows, nullptr, nullptr, nullptr, stream,
+                                                         num_sms);
 }
 
 int launch_quantize_dbias(const void* x, int64_t rows, int64_t cols, int64_t ldx, int fmt, uint8_t* q_cols,
                           float* scale_cols, int64_t sld_cols, uint8_t* q_rows, float* scale_rows, int64_t sld_rows,
                           float* dpart, float* dbias, cudaStream_t stream, int num_sms) {
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
-    if (q_rows) {
-        if (fmt == 0)
-            quantize_cols_kernel<0, true, false, true><<<grid, 256, 0, stream>>>(
-                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows, scale_rows, sld_rows, nullptr, nullptr, dpart);
-        else
-            quantize_cols_kernel<1, true, false, true><<<grid, 256, 0, stream>>>(
-                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows, scale_rows, sld_rows, nullptr, nullptr, dpart);
-    } else {
-        if (fmt == 0)
-            quantize_cols_kernel<0, false, false, true><<<grid, 256, 0, stream>>>(
-                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, nullptr, nullptr, 0, nullptr, nullptr, dpart);
-        else
-            quantize_cols_kernel<1, false, false, true><<<grid, 256, 0, stream>>>(
-                xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, nullptr, nullptr, 0, nullptr, nullptr, dpart);
-    }
-    if (cudaGetLastError() != cudaSuccess) return -3;
+    int rc;
+    if (q_rows)
+        rc = fmt == 0 ? launch_cols<0, true, false, true>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows,
+                                                          scale_rows, sld_rows, nullptr, nullptr, dpart, stream, num_sms)
+                      : launch_cols<1, true, false, true>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, q_rows,
+                                                          scale_rows, sld_rows, nullptr, nullptr, dpart, stream, num_sms);
+    else
+        rc = fmt == 0 ? launch_cols<0, false, false, true>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, nullptr,
+                                                           nullptr, 0, nullptr, nullptr, dpart, stream, num_sms)
+                      : launch_cols<1, false, false, true>(xb, rows, cols, ldx, q_cols, scale_cols, sld_cols, nullptr,
+                                                           nullptr, 0, nullptr, nullptr, dpart, stream, num_sms);
+    if (rc != 0) return rc;
     return launch_bgrad_finalize(dpart, rows / 128, cols, dbias, stream, num_sms);
 }
 
@@ -642,22 +804,15 @@ int launch_tensor_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
     unsigned* am = reinterpret_cast<unsigned*>(amax_out);
     if (am && cudaMemsetAsync(am, 0, sizeof(float), stream) != cudaSuccess) return -3;
     if (q_cols) {
-        dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
-        if (q_rows) {
-            if (fmt == 0)
-                quantize_cols_kernel<0, true, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale, 0,
-                                                                               q_rows, nullptr, 0, amax_in, am);
-            else
-                quantize_cols_kernel<1, true, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale, 0,
-                                                                               q_rows, nullptr, 0, amax_in, am);
-        } else {
-            if (fmt == 0)
-                quantize_cols_kernel<0, false, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale,
-                                                                                0, nullptr, nullptr, 0, amax_in, am);
-            else
-                quantize_cols_kernel<1, false, true><<<grid, 256, 0, stream>>>(xb, rows, cols, ldx, q_cols, scale,
-                                                                                0, nullptr, nullptr, 0, amax_in, am);
-        }
+        if (q_rows)
+            return fmt == 0 ? launch_cols<0, true, true, false>(xb, rows, cols, ldx, q_cols, scale, 0, q_rows, nullptr,
+                                                                0, amax_in, am, nullptr, stream, num_sms)
+                            : launch_cols<1, true, true, false>(xb, rows, cols, ldx, q_cols, scale, 0, q_rows, nullptr,
+                                                                0, amax_in, am, nullptr, stream, num_sms);
+        return fmt == 0 ? launch_cols<0, false, true, false>(xb, rows, cols, ldx, q_cols, scale, 0, nullptr, nullptr, 0,
+                                                             amax_in, am, nullptr, stream, num_sms)
+                        : launch_cols<1, false, true, false>(xb, rows, cols, ldx, q_cols, scale, 0, nullptr, nullptr, 0,
+                                                             amax_in, am, nullptr, stream, num_sms);
     } else {
         const int g = grid_rows(rows, num_sms);
         if (fmt == 0)
