@@ -3,6 +3,8 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "ptx.cuh"
+
 namespace fp8ll {
 
 constexpr int kStatusTimeout = -4;  // FP8LL_ERR_TIMEOUT
@@ -38,52 +40,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   x = clamp(2 sqrt(2/pi) z (1 + 0.044715 z^2), +-80)
 //   gelu(z)  = z / (1 + e^-x)
 //   gelu'(z) = sp + 2 sqrt(2/pi) z (1 + 3 * 0.044715 z^2) sp sm,  sp = s(x), sm = e^-x sp.
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-    uint64_t d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-    return d;
-}
-__device__ __forceinline__ float2 f32x2_split(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
 
 // 2 sqrt(2/pi) z (1 + 0.044715 z^2) for both values, and z^2
 __device__ __forceinline__ uint64_t gelu_arg2(uint64_t z, uint64_t& z2) {
-    const uint64_t c2 = f32x2(1.5957691216057308f, 1.5957691216057308f);  // 2 sqrt(2/pi)
-    z2 = mul2(z, z);
-    return mul2(c2, mul2(z, fma2(z2, f32x2(0.044715f, 0.044715f), f32x2(1.0f, 1.0f))));
+    const uint64_t c2 = pack_f32x2(1.5957691216057308f, 1.5957691216057308f);  // 2 sqrt(2/pi)
+    const uint64_t one = pack_f32x2(1.0f, 1.0f);
+    z2 = mul_f32x2(z, z);
+    return mul_f32x2(c2, mul_f32x2(z, fma_f32x2(z2, pack_f32x2(0.044715f, 0.044715f), one)));
 }
 
 __device__ __forceinline__ float2 gelu_tanh2(float z0, float z1) {
     uint64_t z2;
-    const float2 x = f32x2_split(gelu_arg2(f32x2(z0, z1), z2));
+    const float2 x = unpack_f32x2(gelu_arg2(pack_f32x2(z0, z1), z2));
     const float x0 = fminf(fmaxf(x.x, -80.0f), 80.0f), x1 = fminf(fmaxf(x.y, -80.0f), 80.0f);
     return make_float2(__fdividef(z0, 1.0f + __expf(-x0)), __fdividef(z1, 1.0f + __expf(-x1)));
 }
 
 __device__ __forceinline__ float2 dgelu_tanh2(float z0, float z1) {
-    const uint64_t z = f32x2(z0, z1);
+    const uint64_t z = pack_f32x2(z0, z1);
     uint64_t z2;
-    const float2 x = f32x2_split(gelu_arg2(z, z2));
+    const float2 x = unpack_f32x2(gelu_arg2(z, z2));
     const float x0 = fminf(fmaxf(x.x, -80.0f), 80.0f), x1 = fminf(fmaxf(x.y, -80.0f), 80.0f);
     const float e0 = __expf(-x0), e1 = __expf(-x1);
-    const uint64_t sp = f32x2(__fdividef(1.0f, 1.0f + e0), __fdividef(1.0f, 1.0f + e1));  // s(x)
-    const uint64_t sm = mul2(f32x2(e0, e1), sp);                                          // s(-x)
-    const uint64_t c2 = f32x2(1.5957691216057308f, 1.5957691216057308f);
-    const uint64_t v = mul2(mul2(c2, z), fma2(z2, f32x2(3.0f * 0.044715f, 3.0f * 0.044715f), f32x2(1.0f, 1.0f)));
-    return f32x2_split(fma2(mul2(v, sp), sm, sp));
+    const uint64_t sp = pack_f32x2(__fdividef(1.0f, 1.0f + e0), __fdividef(1.0f, 1.0f + e1));  // s(x)
+    const uint64_t sm = mul_f32x2(pack_f32x2(e0, e1), sp);                                      // s(-x)
+    const uint64_t c2 = pack_f32x2(1.5957691216057308f, 1.5957691216057308f);
+    const uint64_t k3 = pack_f32x2(3.0f * 0.044715f, 3.0f * 0.044715f);
+    const uint64_t v = mul_f32x2(mul_f32x2(c2, z), fma_f32x2(z2, k3, pack_f32x2(1.0f, 1.0f)));
+    return unpack_f32x2(fma_f32x2(mul_f32x2(v, sp), sm, sp));
 }
 
 // Hint that a global cache line will be read soon: fetched into L2 ahead of use.

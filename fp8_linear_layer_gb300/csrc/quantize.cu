@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // of x staged in shared memory as 64 words per row (bf16 pairs), each 32-row
 // band rotated by 8 words so that the column-wise reads of the four 32-row
 // parts hit 32 distinct banks.  Two kernels stage the tiles:
-//   quantize_cols_kernel       one tile per CTA, four CTAs per SM: each thread
+//   quantize_cols_kernel       one tile per CTA, four CTAs per SM (three when
+//                              it writes column codes only): each thread
 //                              loads its eight 16-byte pieces into registers,
 //                              so the row-blocked cast (ROWS) and the tensor's
 //                              amax (TENSOR) are taken from the loaded values.
@@ -152,45 +153,42 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
 // instead of holding 64 values in registers.  quantize_cols_kernel below does
 // the same arithmetic inline (as a shared function it measured 2-6% slower
 // there).
-template <int FMT, bool TENSOR, bool DBIAS>
+template <int FMT, bool DBIAS>
 __device__ __forceinline__ void cast_tile_cols(const uint32_t (*tile)[64], int64_t rows, int64_t cols, int64_t r0,
                                                int64_t c0, int64_t rb, uint8_t* __restrict__ q,
-                                               float* __restrict__ scale, int64_t sld, float inv_t, float s_t,
-                                               float* __restrict__ dpart) {
+                                               float* __restrict__ scale, int64_t sld, float* __restrict__ dpart) {
     const int cp = threadIdx.x >> 2;  // column pair 0..63
     const int p = threadIdx.x & 3;    // 32-row part
     const int64_t c = c0 + 2 * cp;
-    float inv_lo = inv_t, s_lo = s_t, inv_hi = inv_t, s_hi = s_t;
-    if (!TENSOR) {
-        float amax_lo = 0.0f, amax_hi = 0.0f;
-        float sum_lo = 0.0f, sum_hi = 0.0f;  // DBIAS
+    float amax_lo = 0.0f, amax_hi = 0.0f;
+    float sum_lo = 0.0f, sum_hi = 0.0f;  // DBIAS
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
-            amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
-            amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
-            if (DBIAS) {
-                sum_lo = __fadd_rn(sum_lo, bf16_lo(w));
-                sum_hi = __fadd_rn(sum_hi, bf16_hi(w));
-            }
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t w = tile[32 * p + i][(cp + 8 * p) & 63];
+        amax_lo = fmaxf(amax_lo, fabsf(bf16_lo(w)));
+        amax_hi = fmaxf(amax_hi, fabsf(bf16_hi(w)));
+        if (DBIAS) {
+            sum_lo = __fadd_rn(sum_lo, bf16_lo(w));
+            sum_hi = __fadd_rn(sum_hi, bf16_hi(w));
         }
+    }
 #pragma unroll
-        for (int off = 1; off <= 2; off <<= 1) {
-            amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
-            amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
-            if (DBIAS) {
-                // a + b on one lane, b + a on its partner: the same bits on all four
-                sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, off));
-                sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, off));
-            }
+    for (int off = 1; off <= 2; off <<= 1) {
+        amax_lo = fmaxf(amax_lo, __shfl_xor_sync(0xffffffffu, amax_lo, off));
+        amax_hi = fmaxf(amax_hi, __shfl_xor_sync(0xffffffffu, amax_hi, off));
+        if (DBIAS) {
+            // a + b on one lane, b + a on its partner: the same bits on all four
+            sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, off));
+            sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, off));
         }
-        block_scale<FMT>(amax_lo, inv_lo, s_lo);
-        block_scale<FMT>(amax_hi, inv_hi, s_hi);
-        if (DBIAS && p == 0 && c < cols) {
-            // cols is even: c + 1 < cols too
-            dpart[rb * cols + c] = sum_lo;
-            dpart[rb * cols + c + 1] = sum_hi;
-        }
+    }
+    float inv_lo, s_lo, inv_hi, s_hi;
+    block_scale<FMT>(amax_lo, inv_lo, s_lo);
+    block_scale<FMT>(amax_hi, inv_hi, s_hi);
+    if (DBIAS && p == 0 && c < cols) {
+        // cols is even: c + 1 < cols too
+        dpart[rb * cols + c] = sum_lo;
+        dpart[rb * cols + c + 1] = sum_hi;
     }
     if (c < cols) {
         uint32_t wl[8], wh[8];
@@ -213,7 +211,7 @@ __device__ __forceinline__ void cast_tile_cols(const uint32_t (*tile)[64], int64
         dl[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
         dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-        if (!TENSOR && p == 0) {
+        if (p == 0) {
             scale[rb * sld + c] = s_lo;
             scale[rb * sld + c + 1] = s_hi;
         }
@@ -409,8 +407,7 @@ __global__ void __launch_bounds__(256, kPipeCtas) quantize_cols_pipe_kernel(
         cp_async_wait_all_but_one();  // this thread's copies of this tile have landed
         __syncthreads();              // ... and every thread's
         const int64_t rb = t / ncb;
-        cast_tile_cols<FMT, false, DBIAS>(tile, rows, cols, rb * 128, (t - rb * ncb) * 128, rb, q, scale, sld, 1.0f,
-                                          1.0f, dpart);
+        cast_tile_cols<FMT, DBIAS>(tile, rows, cols, rb * 128, (t - rb * ncb) * 128, rb, q, scale, sld, dpart);
     }
 }
 
