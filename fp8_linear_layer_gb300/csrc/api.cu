@@ -183,6 +183,20 @@ bool encode_codes(const uint8_t* q, int64_t ld_q, int64_t rows, int64_t kext, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// TMA descriptor for an MXFP8 scale-atom array (512-byte atoms, the MX cast's
+// layout) viewed as rows of 128 32-bit words: boxes of `atoms` whole atoms.
+bool encode_sf_atoms(const uint8_t* sf, int64_t num_atoms, uint32_t atoms, CUtensorMap* map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(num_atoms)};
+    const cuuint64_t strides[1] = {512};
+    const cuuint32_t box[2] = {128, atoms};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(sf), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool valid_mx_operand(const fp8ll_mx_operand_t* op, int64_t rows, int64_t K) {
     if (!op || !op->q || !op->sf || !valid_fmt(op->fmt)) return false;
     if (!aligned16(op->q) || !aligned16(op->sf)) return false;
@@ -199,21 +213,29 @@ int mx_setup(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const
     int rc = current_device(dev);
     if (rc != FP8LL_OK) return rc;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode_codes(A->q, A->ld_q, M, K, 128, &maps.a) || !encode_codes(B->q, B->ld_q, N, K, kTileN, &maps.b))
+    // CTA pairs: each CTA loads 128 rows of A and 128 of B's 256 tile rows,
+    // its A scale atom and both atoms of B's 256 rows
+    const int64_t sfa_groups = mx_sf_groups(M), sfb_groups = mx_sf_groups(N);
+    if (!encode_codes(A->q, A->ld_q, M, K, 128, &maps.a) ||
+        !encode_codes(B->q, B->ld_q, N, K, kTileN / 2, &maps.b) ||
+        !encode_sf_atoms(A->sf, (K / 128) * sfa_groups, 1, &maps.sa) ||
+        !encode_sf_atoms(B->sf, (K / 128) * sfb_groups, 2, &maps.sb))
         return FP8LL_ERR_LAUNCH;
     std::memset(&p, 0, sizeof(p));
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.num_m_tiles = static_cast<int32_t>((M + kTileM - 1) / kTileM);
     p.num_n_tiles = static_cast<int32_t>((N + kTileN - 1) / kTileN);
-    p.tiles_per_group = p.num_m_tiles * p.num_n_tiles;
+    p.num_m_pairs = static_cast<int32_t>((M + 255) / 256);
+    p.tiles_per_group = p.num_m_pairs * p.num_n_tiles;
     p.num_groups = 1;
     p.groups[0] = GroupEntry{0, static_cast<int32_t>(K / 128), 0, 0};
     p.total_tiles = p.tiles_per_group;
-    // block-scaled instruction descriptor: formats, N >> 3, UE8M0 scales, M >> 4;
-    // the kernel adds the 32-element group id of each MMA for A and B
+    // block-scaled instruction descriptor: formats, N >> 3, UE8M0 scales, M >> 4
+    // (the pair's M = 256); the kernel adds the 32-element group id of each MMA
+    // for A and B
     p.idesc = (static_cast<uint32_t>(A->fmt) << 7) | (static_cast<uint32_t>(B->fmt) << 10) |
-              ((static_cast<uint32_t>(kTileN) >> 3) << 17) | (1u << 23) | ((static_cast<uint32_t>(kTileM) >> 4) << 24);
+              ((static_cast<uint32_t>(kTileN) >> 3) << 17) | (1u << 23) | ((256u >> 4) << 24);
     p.status = (*dev)->status;
     const int starve = g_starve_ms.exchange(0);
     if (starve > 0) {
@@ -224,8 +246,8 @@ int mx_setup(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t* A, const
     }
     p.sfa = A->sf;
     p.sfb = B->sf;
-    p.sfa_groups = mx_sf_groups(M);
-    p.sfb_groups = mx_sf_groups(N);
+    p.sfa_groups = sfa_groups;
+    p.sfb_groups = sfb_groups;
     return FP8LL_OK;
 }
 
@@ -709,7 +731,7 @@ int fp8_mx_gemm_fprop(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
     p.out = out_bf16;
     p.aux = (epi == FP8LL_EPI_BIAS_GELU) ? aux_bf16 : nullptr;
     p.bias = bias_bf16;
-    return launch_gemm_mx(maps, p, epi, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+    return launch_gemm_mx(maps, p, epi, reinterpret_cast<cudaStream_t>(stream)) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }
@@ -733,7 +755,7 @@ int fp8_mx_gemm_dgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
     p.aux = const_cast<void*>(aux_bf16);
     p.workspace = static_cast<float*>(workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_gemm_mx(maps, p, epi, s, grid_for(p, dev)) != 0) return FP8LL_ERR_LAUNCH;
+    if (launch_gemm_mx(maps, p, epi, s) != 0) return FP8LL_ERR_LAUNCH;
     if (epi == FP8LL_EPI_DGELU_BGRAD &&
         launch_bgrad_finalize(static_cast<const float*>(workspace), static_cast<int64_t>(p.num_m_tiles) * 4, N, bgrad,
                               s, dev->num_sms) != 0)
@@ -751,7 +773,7 @@ int fp8_mx_gemm_wgrad(int64_t M, int64_t N, int64_t K, const fp8ll_mx_operand_t*
     if (rc != FP8LL_OK) return rc;
     p.out = out;
     p.accumulate = accumulate;
-    return launch_gemm_mx(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream), grid_for(p, dev)) == 0
+    return launch_gemm_mx(maps, p, kEpiWgrad, reinterpret_cast<cudaStream_t>(stream)) == 0
                ? FP8LL_OK
                : FP8LL_ERR_LAUNCH;
 }

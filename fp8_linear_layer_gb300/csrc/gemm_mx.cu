@@ -1,24 +1,32 @@
-// gemm_mx.cu -- MXFP8 GEMM for sm_103a: the scales are applied by the tensor
-// core (tcgen05.mma kind::mxf8f6f4 block_scale, one UE8M0 power-of-two scale
-// per 32 K-elements of every row of A and B), so the fp32 accumulator stays in
-// tensor memory for the whole K range and no software promotion exists.
+// gemm_mx.cu -- MXFP8 GEMM for sm_103a on CTA pairs: the scales are applied
+// by the tensor core (tcgen05.mma kind::mxf8f6f4 block_scale, one UE8M0
+// power-of-two scale per 32 K-elements of every row of A and B), so the fp32
+// accumulator stays in tensor memory for the whole K range and no software
+// promotion exists.
 //
-// Same tiling as the 1x128 kernel (128 x 256 output tiles, 128-deep K blocks,
-// persistent CTAs), same epilogues (bias / GELU, GELU derivative with bias
-// gradient, fp32 out (+)=).  Per CTA:
-//   warp 0      TMA producer: A and B code boxes (128-byte swizzle) plus the
-//               block's scale atoms (512 B for A, 1 KB for B, untiled bulk
-//               copies) into one 4-stage ring.
-//   warp 1      TMEM owner and MMA issuer: per K block, three tcgen05.cp copy
-//               the scale atoms into a tensor-memory scale slot (4 slots of
-//               16 columns, 12 used: lane l, column c = the four 32-element
-//               scales of row l + 32c, B's rows 128..255 four columns
-//               further), then
-//               four block-scaled MMAs (M=128, N=256, K=32, scale id = the
-//               32-element group) accumulate into one 256-column accumulator.
-//   warps 4-11  epilogue: once per tile, the accumulator is read (16x256b
-//               fragments, as in the 1x128 kernel), handed back to the MMA
-//               warp, and stored through the same epilogue functions.
+// Clusters of two CTAs on two SMs share each MMA (cta_group::2, M = 256,
+// N = 256), as the per-tensor kernel does: each CTA loads its 128 rows of A,
+// half of B's 256 rows and, per 128-deep K block, the scale atoms its half of
+// the MMA reads from its own tensor memory -- the 512-byte atom of its A rows
+// and both atoms of B's 256 rows (a probe on the GPU showed each CTA's half of
+// a pair's block-scaled MMA takes A's scales for its rows and all of B's from
+// its own tensor memory, and tcgen05.cp.cta_group::2 fills each CTA's tensor
+// memory from that CTA's shared memory).  Per CTA, 3 warpgroups:
+//   warp 0      TMA producer: A and B code boxes (128-byte swizzle) and the
+//               scale atoms (as 128-word rows of a 2-D map over the atom
+//               array) into a 6-stage ring; both CTAs' bytes are counted on
+//               the leader's (rank 0's) stage barrier.
+//   warp 1      TMEM owner (the pair allocates together) and, in the leader,
+//               MMA issuer: per K block three tcgen05.cp copy the block's
+//               scale atoms into one of four 16-column tensor-memory scale
+//               slots of both CTAs (lane l, column c = the four 32-element
+//               scales of row l + 32c; B's rows 128..255 four columns
+//               further), then four block-scaled MMAs (M=256, N=256, K=32,
+//               scale id = the 32-element group) accumulate into one
+//               256-column accumulator per CTA.
+//   warps 4-11  epilogue: once per tile each CTA reads its 128 rows of the
+//               accumulator (16x256b fragments), hands it back to the leader
+//               and stores through the epilogues of the 1x128 kernel.
 // The scale atoms are the layout the MX cast writes (see quantize.cu).
 //
 // The per-tensor scaled GEMM (one scale per operand, no scale atoms) runs on
@@ -27,34 +35,31 @@
 
 namespace fp8ll {
 
-constexpr int kMxStages = 4;
+constexpr int kMxStages = 6;
 constexpr int kMxSfSlots = 4;
 constexpr uint32_t kMxSfCol0 = 256;   // accumulator in columns 0..255
 constexpr uint32_t kMxSfSlotCols = 16;
 constexpr uint32_t kMxTmemCols = 512;
 static_assert(kMxSfCol0 + kMxSfSlots * kMxSfSlotCols <= kMxTmemCols, "TMEM budget");
+constexpr int kMxRows = 2 * kBM;     // output rows of a pair's tile
+constexpr int kMxBRows = kBN / 2;    // rows of B each CTA loads
+constexpr int kMxRaster = kRasterM / 2;
+constexpr uint32_t kMxStageBytes = (kBM + kMxBRows) * kBK + 512 + 1024;  // one CTA's bytes per K block
 
 struct __align__(1024) MxSmem {
+    uint8_t b[kMxStages][kMxBRows * kBK];
     uint8_t a[kMxStages][kBM * kBK];
-    uint8_t b[kMxStages][kBN * kBK];
-    uint8_t sfa[kMxStages][512];
-    uint8_t sfb[kMxStages][1024];
-    uint64_t full[kMxStages];
-    uint64_t empty[kMxStages];
+    uint8_t sfa[kMxStages][512];   // the atom of this CTA's 128 rows of A
+    uint8_t sfb[kMxStages][1024];  // both atoms of the pair's 256 rows of B
+    uint64_t full[kMxStages];      // leader: both CTAs' bytes of stage s have landed
+    uint64_t empty[kMxStages];     // stage s read by the pair's copies and MMAs
     uint64_t acc_full[1];
-    uint64_t acc_empty[1];
+    uint64_t acc_empty[1];         // leader: both CTAs' epilogue warps have read the accumulator
     uint64_t drain;
     uint32_t tmem_base;
 };
 constexpr size_t kMxSmemBytes = sizeof(MxSmem) + 1024;
 static_assert(kMxSmemBytes <= 232448, "shared memory budget");
-
-// untiled bulk copy global -> shared, completion counted on an mbarrier
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
 
 // no-swizzle shared-memory descriptor for a 32-row x 16-byte scale atom
 // (8-row x 16-byte core matrices, 128 bytes apart)
@@ -63,21 +68,34 @@ __device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
            (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
 }
 
-__device__ __forceinline__ void sf_copy(uint32_t taddr, uint32_t saddr) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sf_desc(saddr)) : "memory");
+// each CTA's atom at this shared-memory offset -> the same columns of its own tensor memory
+__device__ __forceinline__ void sf_copy_pair(uint32_t taddr, uint32_t saddr) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sf_desc(saddr)) : "memory");
 }
 
-__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
-                                       uint32_t sfb, uint32_t accumulate) {
+__device__ __forceinline__ void mma_mx_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
         : "memory");
 }
 
+// pair-tile index -> (pair-row tile, n tile), as decode_tile over 256-row tiles
+__device__ __forceinline__ void decode_mx_tile(const GemmParams& p, int t, int& mt, int& nt) {
+    const int band_tiles = kMxRaster * p.num_n_tiles;
+    const int band = t / band_tiles;
+    const int first_m = band * kMxRaster;
+    const int rem_m = p.num_m_pairs - first_m;
+    const int bm = rem_m < kMxRaster ? rem_m : kMxRaster;
+    const int r = t - band * band_tiles;
+    mt = first_m + r % bm;
+    nt = r / bm;
+}
+
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ TensorMaps maps, const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     MxSmem& sm = *reinterpret_cast<MxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -86,8 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t budget = p.budget_ns;
     const int nkb = p.groups[0].nkb;
-    // one 256-column accumulator: columns 256.. hold the scale slots
-    constexpr int kAccBufs = 1;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMxStages; ++s) {
@@ -95,16 +115,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
         mbar_init(smem_addr(&sm.acc_full[0]), 1);
-        mbar_init(smem_addr(&sm.acc_empty[0]), kEpiWarps);
+        mbar_init(smem_addr(&sm.acc_empty[0]), 2 * kEpiWarps);
         mbar_init(smem_addr(&sm.drain), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(&sm.tmem_base), kMxTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_addr(&sm.tmem_base), kMxTmemCols);
+        tmem_relinquish_pair();
     }
+    // both CTAs' barriers initialised and tensor memory allocated before either signals the other
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
 
@@ -114,34 +135,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&maps.a);
             tma_prefetch_desc(&maps.b);
+            tma_prefetch_desc(&maps.sa);
+            tma_prefetch_desc(&maps.sb);
             int s = 0;
             uint32_t ph = 0;
             int n_issued = 0;
             bool ok = true;
             if (!p.debug_starve) {
-                for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-                    int g, mt, nt;
-                    decode_tile(p, t, g, mt, nt);
-                    const int m0 = mt * kBM, n0 = nt * kBN;
+                for (int t = pair; t < p.total_tiles && ok; t += num_pairs) {
+                    int mt, nt;
+                    decode_mx_tile(p, t, mt, nt);
+                    const int m0 = mt * kMxRows + static_cast<int>(rank) * kBM;
+                    const int nb0 = nt * kBN + static_cast<int>(rank) * kMxBRows;
                     for (int kb = 0; kb < nkb; ++kb) {
                         if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, budget)) {
                             ok = false;
                             break;
                         }
                         const uint32_t fb = smem_addr(&sm.full[s]);
-                        mbar_arrive_expect_tx(fb, kBM * kBK + kBN * kBK + 512 + 1024);
-                        tma_load_2d(smem_addr(sm.a[s]), &maps.a, fb, kb * kBK, m0);
-                        tma_load_2d(smem_addr(sm.b[s]), &maps.b, fb, kb * kBK, n0);
-                        bulk_load(smem_addr(sm.sfa[s]), p.sfa + (static_cast<int64_t>(kb) * p.sfa_groups + mt) * 512,
-                                  512, fb);
-                        bulk_load(smem_addr(sm.sfb[s]),
-                                  p.sfb + (static_cast<int64_t>(kb) * p.sfb_groups + 2 * nt) * 512, 1024, fb);
+                        if (leader) mbar_arrive_expect_tx(fb, 2 * kMxStageBytes);
+                        const uint32_t fbl = mapa_shared(fb, 0);
+                        tma_load_2d_pair(smem_addr(sm.a[s]), &maps.a, fbl, kb * kBK, m0);
+                        tma_load_2d_pair(smem_addr(sm.b[s]), &maps.b, fbl, kb * kBK, nb0);
+                        // scale atoms: rows of 128 words; A's atom of this CTA's 128-row group,
+                        // both atoms of the tile's 256 rows of B
+                        tma_load_2d_pair(smem_addr(sm.sfa[s]), &maps.sa, fbl, 0,
+                                         static_cast<int32_t>(kb * p.sfa_groups + 2 * mt + static_cast<int>(rank)));
+                        tma_load_2d_pair(smem_addr(sm.sfb[s]), &maps.sb, fbl, 0,
+                                         static_cast<int32_t>(kb * p.sfb_groups + 2 * nt));
                         ++n_issued;
                         ring_advance<kMxStages>(s, ph);
                     }
                 }
             }
             if (ok) {
+                // every stage must be released by the pair's MMAs before exit
                 for (int i = 0; i < kMxStages; ++i) {
                     if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, budget)) ok = false;
                     ring_advance<kMxStages>(s, ph);
@@ -149,61 +177,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 record_status(p.status, kStatusTimeout);
-                for (int i = 1; i <= (n_issued < kMxStages ? n_issued : kMxStages); ++i) {
-                    int si = s - i;
-                    uint32_t pi = ph;
-                    if (si < 0) {
-                        si += kMxStages;
-                        pi ^= 1u;
+                // the leader's stage barriers count both CTAs' bytes: the loads
+                // still in flight land before the leader (and, at the final
+                // cluster barrier, the peer) leaves
+                if (leader) {
+                    for (int i = 1; i <= (n_issued < kMxStages ? n_issued : kMxStages); ++i) {
+                        int si = s - i;
+                        uint32_t pi = ph;
+                        if (si < 0) {
+                            si += kMxStages;
+                            pi ^= 1u;
+                        }
+                        mbar_wait(smem_addr(&sm.full[si]), pi, budget);
                     }
-                    mbar_wait(smem_addr(&sm.full[si]), pi, budget);
                 }
             }
         }
     } else if (warp == 1) {
-        // -------------------------------------------------------- MMA issuer
-        int s = 0, ab = 0;
-        uint32_t ph = 0, aph = 0;
-        uint32_t slot = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-            // the accumulator must have been read by the epilogue of the tile that used it last
-            ok = mbar_wait_warp(smem_addr(&sm.acc_empty[ab]), aph ^ 1u, budget);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * kBN);
-            for (int kb = 0; kb < nkb; ++kb) {
-                ok = mbar_wait_warp(smem_addr(&sm.full[s]), ph, budget);
+        // -------------------------------------------- MMA issuer (leader only)
+        if (leader) {
+            int s = 0;
+            uint32_t ph = 0, aph = 0;
+            uint32_t slot = 0;
+            bool ok = true;
+            for (int t = pair; t < p.total_tiles && ok; t += num_pairs) {
+                // both CTAs' epilogues must have read the accumulator's last tile
+                ok = mbar_wait_warp(smem_addr(&sm.acc_empty[0]), aph ^ 1u, budget);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t adesc = smem_desc_k_sw128(smem_addr(sm.a[s]));
-                    const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sm.b[s]));
-                    const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
-                    sf_copy(tsf, smem_addr(sm.sfa[s]));
-                    sf_copy(tsf + 4, smem_addr(sm.sfb[s]));
-                    sf_copy(tsf + 8, smem_addr(sm.sfb[s] + 512));
+                for (int kb = 0; kb < nkb; ++kb) {
+                    ok = mbar_wait_warp(smem_addr(&sm.full[s]), ph, budget);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint64_t adesc = smem_desc_k_sw128(smem_addr(sm.a[s]));
+                        const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sm.b[s]));
+                        const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
+                        sf_copy_pair(tsf, smem_addr(sm.sfa[s]));
+                        sf_copy_pair(tsf + 4, smem_addr(sm.sfb[s]));
+                        sf_copy_pair(tsf + 8, smem_addr(sm.sfb[s] + 512));
 #pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k) {
-                        const uint32_t idesc =
-                            p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-                        mma_mx(dacc, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
-                               (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kBK / 32; ++k) {
+                            const uint32_t idesc =
+                                p.idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+                            mma_mx_pair(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc, tsf, tsf + 4,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit_pair(smem_addr(&sm.empty[s]), 0x3);
+                        if (kb == nkb - 1) mma_commit_pair(smem_addr(&sm.acc_full[0]), 0x3);
                     }
-                    mma_commit(smem_addr(&sm.empty[s]));
-                    if (kb == nkb - 1) mma_commit(smem_addr(&sm.acc_full[ab]));
+                    __syncwarp();
+                    ring_advance<kMxStages>(s, ph);
+                    slot = (slot + 1) % kMxSfSlots;
                 }
-                __syncwarp();
-                ring_advance<kMxStages>(s, ph);
-                slot = (slot + 1) % kMxSfSlots;
+                aph ^= 1u;
             }
-            ring_advance<kAccBufs>(ab, aph);
+            if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
+            // every MMA of the pair completes before either CTA frees its memory
+            if (lane == 0) mma_commit_pair(smem_addr(&sm.drain), 0x3);
+            __syncwarp();
+            mbar_wait(smem_addr(&sm.drain), 0, budget);
+            __syncwarp();
         }
-        if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
-        if (lane == 0) mma_commit(smem_addr(&sm.drain));
-        __syncwarp();
-        mbar_wait(smem_addr(&sm.drain), 0, budget);
-        __syncwarp();
     } else if (warp >= kFirstEpiWarp) {
         // ---------------------------------------------------------- epilogue
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
@@ -212,13 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;
         const int g8 = lane >> 2;
         const int cq = lane & 3;
-        int ab = 0;
+        const uint32_t acc_empty_leader = mapa_shared(smem_addr(&sm.acc_empty[0]), 0);
         uint32_t aph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-            int g, mt, nt;
-            decode_tile(p, t, g, mt, nt);
-            const int m0 = mt * kBM, n0 = nt * kBN;
+        for (int t = pair; t < p.total_tiles && ok; t += num_pairs) {
+            int mt, nt;
+            decode_mx_tile(p, t, mt, nt);
+            const int m0 = mt * kMxRows + static_cast<int>(rank) * kBM, n0 = nt * kBN;
             if (EPI == kEpiDgelu || EPI == kEpiDgeluBgrad) {
                 const int prow = m0 + q * 32 + g8 + 8 * cq;
                 const int pc0 = n0 + half * kHalfN;
@@ -230,12 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     prefetch_l2(zrow + pc1);
                 }
             }
-            ok = mbar_wait_warp(smem_addr(&sm.acc_full[ab]), aph, budget);
+            ok = mbar_wait_warp(smem_addr(&sm.acc_full[0]), aph, budget);
             if (!ok) break;
             tc_fence_after();
             uint64_t acc[4 * kChunks];
-            const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>(ab * kBN + half * kHalfN);
+            const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(half * kHalfN);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 uint64_t plo[8], phi[8];
@@ -249,11 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[4 * c + 3] = phi[2 * i + 1];
                 }
             }
-            // the tile's sums are in registers: the accumulator goes back to the MMA warp
+            // the tile's sums are in registers: the accumulator goes back to the leader
             tc_fence_before();
             __syncwarp();
-            mbar_arrive_lane0(smem_addr(&sm.acc_empty[ab]), lane);
-            ring_advance<kAccBufs>(ab, aph);
+            mbar_arrive_remote_lane0(acc_empty_leader, lane);
+            aph ^= 1u;
+            // the peer of a pair whose tile ends inside the leader's rows holds
+            // only rows outside the matrix and stores nothing
+            if (m0 >= p.M) continue;
             const int row0 = m0 + q * 32 + g8;
             const int col0 = n0 + half * kHalfN + 2 * cq;
             if (EPI == kEpiWgrad) {
@@ -261,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (EPI == kEpiNone || EPI == kEpiBias || EPI == kEpiBiasGelu) {
                 store_fprop<EPI>(p, row0, col0, acc);
             } else {
-                float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(mt) * 4 + q) * p.N
+                float* band = (EPI == kEpiDgeluBgrad) ? p.workspace + (static_cast<int64_t>(m0 / kBM) * 4 + q) * p.N
                                                       : nullptr;
                 store_dgrad<EPI == kEpiDgeluBgrad, false>(p, row0, col0, acc, band, lane, nullptr);
             }
@@ -269,16 +306,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
     }
 
+    // neither CTA leaves (or frees its tensor memory) while the other may still
+    // use its shared memory, tensor memory or barriers
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, kMxTmemCols);
+    if (warp == 1) {
+        // the leader waited for the pair's MMAs above; the peer's drain barrier
+        // received the same commit
+        if (!leader) mbar_wait_warp(smem_addr(&sm.drain), 0, budget);
+        tmem_dealloc_pair(tmem_base, kMxTmemCols);
+    }
 }
 
 template <int EPI>
-int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid) {
+int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream) {
     auto kern = gemm_mx_kernel<EPI>;
     static unsigned long long configured = 0;
+    static int pairs_on[64] = {0};  // resident CTA pairs per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -3;
     if (!(configured & (1ull << dev))) {
@@ -287,20 +333,34 @@ int launch_mx_impl(const TensorMaps& maps, const GemmParams& p, cudaStream_t str
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kMxSmemBytes)) != cudaSuccess)
             return -3;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kMxSmemBytes;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -3;
+            n = sms / 2;
+        }
+        pairs_on[dev] = n;
         configured |= 1ull << dev;
     }
+    const int pairs = pairs_on[dev];
+    const int grid = 2 * (p.total_tiles < pairs ? p.total_tiles : pairs);
     kern<<<grid, kThreads, kMxSmemBytes, stream>>>(maps, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid) {
+int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream) {
     switch (epi) {
-        case kEpiNone: return launch_mx_impl<kEpiNone>(maps, p, stream, grid);
-        case kEpiBias: return launch_mx_impl<kEpiBias>(maps, p, stream, grid);
-        case kEpiBiasGelu: return launch_mx_impl<kEpiBiasGelu>(maps, p, stream, grid);
-        case kEpiDgelu: return launch_mx_impl<kEpiDgelu>(maps, p, stream, grid);
-        case kEpiDgeluBgrad: return launch_mx_impl<kEpiDgeluBgrad>(maps, p, stream, grid);
-        case kEpiWgrad: return launch_mx_impl<kEpiWgrad>(maps, p, stream, grid);
+        case kEpiNone: return launch_mx_impl<kEpiNone>(maps, p, stream);
+        case kEpiBias: return launch_mx_impl<kEpiBias>(maps, p, stream);
+        case kEpiBiasGelu: return launch_mx_impl<kEpiBiasGelu>(maps, p, stream);
+        case kEpiDgelu: return launch_mx_impl<kEpiDgelu>(maps, p, stream);
+        case kEpiDgeluBgrad: return launch_mx_impl<kEpiDgeluBgrad>(maps, p, stream);
+        case kEpiWgrad: return launch_mx_impl<kEpiWgrad>(maps, p, stream);
         default: return -3;
     }
 }

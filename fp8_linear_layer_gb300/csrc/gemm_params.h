@@ -32,7 +32,7 @@ struct GroupEntry {
 struct GemmParams {
     int32_t M, N;
     int32_t num_m_tiles, num_n_tiles;  // 128-row and 256-column tiles
-    int32_t num_m_pairs;               // per-tensor GEMM: 256-row tiles of a CTA pair
+    int32_t num_m_pairs;               // MXFP8 / per-tensor GEMMs: 256-row tiles of a CTA pair
     int32_t tiles_per_group;
     int32_t num_groups;
     int32_t total_tiles;

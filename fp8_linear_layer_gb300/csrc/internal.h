@@ -41,9 +41,9 @@ int launch_cast_f32(const float* x, int64_t n, int fmt, uint8_t* q, cudaStream_t
 int launch_gemm_fprop(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_gemm_dgrad(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
 int launch_gemm_wgrad(const TensorMaps& maps, const GemmParams& p, cudaStream_t stream, int grid);
-int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream, int grid);
-// The per-tensor GEMM runs on CTA pairs over 256 x 256 tiles (p.num_m_pairs,
-// p.tiles_per_group in pair tiles) and sizes its own grid.
+// The MXFP8 and per-tensor GEMMs run on CTA pairs over 256 x 256 tiles
+// (p.num_m_pairs, p.tiles_per_group in pair tiles) and size their own grids.
+int launch_gemm_mx(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream);
 int launch_gemm_tensor(const TensorMaps& maps, const GemmParams& p, int epi, cudaStream_t stream);
 int launch_bgrad_finalize(const float* ws, int64_t num_bands, int64_t N, float* bgrad, cudaStream_t stream,
                           int num_sms);
