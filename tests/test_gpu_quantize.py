@@ -150,3 +150,22 @@ def test_strided_input(fp8):
     torch.cuda.synchronize()
     qo, so = oracle.quantize(workloads.bits(x.contiguous()), 0)
     assert np.array_equal(t.q.cpu().numpy(), qo)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_transposed_many_tiles_per_cta_ragged(fp8, fmt):
+    # 64 row blocks x 33 column blocks (the last 8 columns wide) on a strided
+    # input: more tiles than the persistent cast keeps resident CTAs, so each
+    # CTA casts several tiles through both shared-memory stages and the ragged
+    # column block lands on different CTAs at different iterations.  Every code
+    # and scale is checked.
+    rows, cols, pad = 8192, 4104, 24
+    assert (rows // 128) * ((cols + 127) // 128) > 4 * 152 * 3
+    base = workloads.normal_bf16((rows, cols + pad), 500 + fmt, "mt", std=0.7)
+    x = base.cuda()[:, :cols]
+    t = fp8.quantize(x, fmt, transpose=True)
+    torch.cuda.synchronize()
+    qo, so = oracle.quantize(workloads.bits(base[:, :cols].contiguous()), fmt, transpose=True)
+    q, s = t.q.cpu().numpy(), t.scale.cpu().numpy()[:, :cols]
+    assert np.array_equal(q, qo), "codes differ at %s" % (np.argwhere(q != qo)[:5].tolist(),)
+    assert np.array_equal(s.view(np.uint32), so.view(np.uint32)), "scale bits differ"

@@ -142,3 +142,21 @@ def test_train_step_with_the_bias_gradient_in_the_cast(fp8, input_grad):
     db = st.db.cpu().double().numpy()
     assert np.all(np.abs(db - dzo.sum(0)) <= tol)
     assert np.all(np.abs(db - ref.db.cpu().double().numpy()) <= 2 * tol)
+
+
+def test_many_tiles_per_cta_ragged(fp8):
+    # more tiles than the persistent cast keeps resident CTAs, a ragged last
+    # column block and a strided input: codes and scales exact against the
+    # oracle, db within the bound above in every column
+    rows, cols, pad = 8192, 4104, 24
+    base = workloads.normal_bf16((rows, cols + pad), 340, "mtd", std=0.02)
+    x = base.cuda()[:, :cols]
+    _, out_t, db = fp8.quantize_dbias(x, E5M2)
+    torch.cuda.synchronize()
+    xb = workloads.bits(base[:, :cols].contiguous())
+    qo, so = oracle.quantize(xb, E5M2, transpose=True)
+    assert np.array_equal(out_t.q.cpu().numpy(), qo)
+    assert np.array_equal(out_t.scale.cpu().numpy()[:, :cols].view(np.uint32), so.view(np.uint32))
+    xd = oracle.bf16_to_f64(xb)
+    got = db.cpu().double().numpy()
+    assert np.all(np.abs(got - oracle.colsum(xd)) <= db_bound(rows, xd))
