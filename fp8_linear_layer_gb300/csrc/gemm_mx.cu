@@ -17,13 +17,20 @@
 //               array) into a 6-stage ring; both CTAs' bytes are counted on
 //               the leader's (rank 0's) stage barrier.
 //   warp 1      TMEM owner (the pair allocates together) and, in the leader,
-//               MMA issuer: per K block three tcgen05.cp copy the block's
-//               scale atoms into one of four 16-column tensor-memory scale
-//               slots of both CTAs (lane l, column c = the four 32-element
-//               scales of row l + 32c; B's rows 128..255 four columns
-//               further), then four block-scaled MMAs (M=256, N=256, K=32,
-//               scale id = the 32-element group) accumulate into one
-//               256-column accumulator per CTA.
+//               MMA issuer: per K block, once the stage and its scales are
+//               in place, four block-scaled MMAs (M=256, N=256, K=32, scale
+//               id = the 32-element group) accumulate into one 256-column
+//               accumulator per CTA.
+//   warp 3      in the leader, scale copier: as each stage lands, three
+//               tcgen05.cp copy its scale atoms into that stage's 16-column
+//               tensor-memory slot of both CTAs (lane l, column c = the four
+//               32-element scales of row l + 32c; B's rows 128..255 four
+//               columns further) and a commit tells the MMA issuer.  Copies
+//               issued by the MMA thread itself, ahead of each block's MMAs,
+//               cost the GEMMs 14-17% (they hold up the MMA issue); from this
+//               warp the results are bit-identical.  One slot per stage: a
+//               slot is refilled only after its stage was, i.e. after the
+//               MMAs that read it completed.
 //   warps 4-11  epilogue: once per tile each CTA reads its 128 rows of the
 //               accumulator (16x256b fragments), hands it back to the leader
 //               and stores through the epilogues of the 1x128 kernel.
@@ -36,7 +43,7 @@
 namespace fp8ll {
 
 constexpr int kMxStages = 6;
-constexpr int kMxSfSlots = 4;
+constexpr int kMxSfSlots = kMxStages;  // scale slot s belongs to stage s
 constexpr uint32_t kMxSfCol0 = 256;   // accumulator in columns 0..255
 constexpr uint32_t kMxSfSlotCols = 16;
 constexpr uint32_t kMxTmemCols = 512;
@@ -56,6 +63,8 @@ struct __align__(1024) MxSmem {
     uint64_t acc_full[1];
     uint64_t acc_empty[1];         // leader: both CTAs' epilogue warps have read the accumulator
     uint64_t drain;
+    uint64_t sf_full[kMxStages];   // leader: stage s's scales are in both CTAs' tensor memory
+    uint64_t sf_drain;             // leader: the copier's last copies completed
     uint32_t tmem_base;
 };
 constexpr size_t kMxSmemBytes = sizeof(MxSmem) + 1024;
@@ -117,6 +126,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&sm.acc_full[0]), 1);
         mbar_init(smem_addr(&sm.acc_empty[0]), 2 * kEpiWarps);
         mbar_init(smem_addr(&sm.drain), 1);
+        for (int s = 0; s < kMxStages; ++s) mbar_init(smem_addr(&sm.sf_full[s]), 1);
+        mbar_init(smem_addr(&sm.sf_drain), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -198,7 +209,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (leader) {
             int s = 0;
             uint32_t ph = 0, aph = 0;
-            uint32_t slot = 0;
             bool ok = true;
             for (int t = pair; t < p.total_tiles && ok; t += num_pairs) {
                 // both CTAs' epilogues must have read the accumulator's last tile
@@ -206,16 +216,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 for (int kb = 0; kb < nkb; ++kb) {
-                    ok = mbar_wait_warp(smem_addr(&sm.full[s]), ph, budget);
+                    ok = mbar_wait2_warp(smem_addr(&sm.full[s]), ph, smem_addr(&sm.sf_full[s]), ph, budget);
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
                         const uint64_t adesc = smem_desc_k_sw128(smem_addr(sm.a[s]));
                         const uint64_t bdesc = smem_desc_k_sw128(smem_addr(sm.b[s]));
-                        const uint32_t tsf = tmem_base + kMxSfCol0 + slot * kMxSfSlotCols;
-                        sf_copy_pair(tsf, smem_addr(sm.sfa[s]));
-                        sf_copy_pair(tsf + 4, smem_addr(sm.sfb[s]));
-                        sf_copy_pair(tsf + 8, smem_addr(sm.sfb[s] + 512));
+                        const uint32_t tsf = tmem_base + kMxSfCol0 + static_cast<uint32_t>(s) * kMxSfSlotCols;
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k) {
                             const uint32_t idesc =
@@ -228,7 +235,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                     ring_advance<kMxStages>(s, ph);
-                    slot = (slot + 1) % kMxSfSlots;
                 }
                 aph ^= 1u;
             }
@@ -237,6 +243,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mma_commit_pair(smem_addr(&sm.drain), 0x3);
             __syncwarp();
             mbar_wait(smem_addr(&sm.drain), 0, budget);
+            __syncwarp();
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------- scale copier (leader only)
+        if (leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = pair; t < p.total_tiles && ok; t += num_pairs) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    // stage s of this block landed in both CTAs; its slot's last
+                    // readers (the MMAs of the stage's previous use) completed
+                    // before the producer refilled it
+                    ok = mbar_wait_warp(smem_addr(&sm.full[s]), ph, budget);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t tsf = tmem_base + kMxSfCol0 + static_cast<uint32_t>(s) * kMxSfSlotCols;
+                        sf_copy_pair(tsf, smem_addr(sm.sfa[s]));
+                        sf_copy_pair(tsf + 4, smem_addr(sm.sfb[s]));
+                        sf_copy_pair(tsf + 8, smem_addr(sm.sfb[s] + 512));
+                        mma_commit_pair(smem_addr(&sm.sf_full[s]), 0x1);
+                    }
+                    __syncwarp();
+                    ring_advance<kMxStages>(s, ph);
+                }
+            }
+            if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
+            // the copies complete before either CTA frees its tensor memory
+            if (lane == 0) mma_commit_pair(smem_addr(&sm.sf_drain), 0x1);
+            __syncwarp();
+            mbar_wait(smem_addr(&sm.sf_drain), 0, budget);
             __syncwarp();
         }
     } else if (warp >= kFirstEpiWarp) {
