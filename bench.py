@@ -38,31 +38,37 @@ FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor-core ratio on this part
 KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "common.cuh", "cast_rule.cuh", "gemm_params.h", "gemm_fprop.cu", "gemm_dgrad.cu",
                   "gemm_wgrad.cu")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fp8_kernel_m8192_k4096_n14336_traffic.md")
+# the CTA-pair kernels share the epilogue sources of the 1x128 kernel
+RECIPE_SOURCES = {"block128": KERNEL_SOURCES,
+                  "mx": KERNEL_SOURCES[:5] + ("gemm_mx.cu",),
+                  "tensor": KERNEL_SOURCES[:5] + ("gemm_tensor.cu",)}
+RECIPE_TRAFFIC = {"mx": os.path.join(ROOT, "profiles", "gemm_mx_kernel_m8192_k4096_n14336_traffic.md"),
+                  "tensor": os.path.join(ROOT, "profiles", "gemm_tensor_kernel_m8192_k4096_n14336_traffic.md")}
 
 
-def kernel_source_digest():
-    """sha256 over the GEMM kernel's source files (the DRAM-traffic summary
-    applies only to the build it was measured on)."""
+def kernel_source_digest(recipe="block128"):
+    """sha256 over the recipe's GEMM kernel source files (a DRAM-traffic
+    summary applies only to the build it was measured on)."""
     import hashlib
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in RECIPE_SOURCES[recipe]:
         with open(os.path.join(ROOT, "fp8_linear_layer_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def measured_traffic():
+def measured_traffic(recipe="block128"):
     """DRAM bytes per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum,
-    averaged over the step's three launches) from the committed ncu summary,
-    or None when the kernel sources changed since it was taken."""
+    averaged over the step's three launches) from the recipe's committed ncu
+    summary, or None when its kernel sources changed since it was taken."""
     import re
     try:
-        text = open(TRAFFIC_SUMMARY).read()
+        text = open(TRAFFIC_SUMMARY if recipe == "block128" else RECIPE_TRAFFIC[recipe]).read()
     except OSError:
         return None
     sha = re.search(r"sources_sha256:\s*([0-9a-f]{64})", text)
     val = re.search(r"bytes_per_launch:\s*([0-9]+)", text)
-    if not sha or not val or sha.group(1) != kernel_source_digest():
+    if not sha or not val or sha.group(1) != kernel_source_digest(recipe):
         return None
     return int(val.group(1))
 
@@ -493,8 +499,9 @@ def run_ours(args):
                          + " (fprop, dgrad, wgrad launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                          "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16 ratio)" % (peak_src, FP8_OVER_BF16),
-                         "traffic": measured_traffic()
-                         if default_size and args.recipe == "block128" and args.bias_grad == "cast" else None,
+                         # the summaries were taken on the default step of each recipe
+                         "traffic": measured_traffic(args.recipe)
+                         if default_size and (args.recipe == "tensor" or args.bias_grad == "cast") else None,
                          "traffic_unit": "bytes",
                          "avg_gemm_ms": avg_gemm_ms},
             "e2e": e2e,

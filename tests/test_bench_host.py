@@ -26,8 +26,16 @@ def test_traffic_follows_the_source_digest(tmp_path, monkeypatch):
 
 
 def test_committed_traffic_summary_matches_these_sources():
-    # the committed summary was captured on the kernel sources in this tree
+    # the committed summaries were captured on the kernel sources in this tree
     assert bench.measured_traffic() is not None
+    assert bench.measured_traffic("mx") is not None
+    assert bench.measured_traffic("tensor") is not None
+
+
+def test_each_recipe_digest_covers_its_own_kernel():
+    assert bench.kernel_source_digest("mx") != bench.kernel_source_digest("tensor")
+    assert "gemm_mx.cu" in bench.RECIPE_SOURCES["mx"] and "gemm_tensor.cu" in bench.RECIPE_SOURCES["tensor"]
+    assert "gemm_kernel.cuh" in bench.RECIPE_SOURCES["mx"]  # the shared epilogues
 
 
 def test_reference_arm_line(tmp_path):
