@@ -147,3 +147,21 @@ def test_tensor_wgrad_full_size(fp8):
     want = oracle.wgrad(acc, pre.double().numpy()[np.ix_(ri, ci)])
     got = _sel(dW, ri, ci).cpu().double().numpy()
     assert_within(got, want, FULL_C * S + f32_ulp(want), "dW")
+
+
+def test_mx_input_grad_full_size(fp8):
+    # dX = dZ W on MXFP8 operands: dZ cast by rows, W down its columns
+    m, k, n = TS["m"], TS["k"], TS["n"]
+    dz = workloads.normal_bf16((m, n), 1707, "dz", std=1e-2)
+    w = workloads.normal_bf16((n, k), 1707, "w", std=0.02)
+    A = fp8.mx_quantize(dz.cuda(), E5M2)
+    Bt = fp8.mx_quantize(w.cuda(), E4M3, transpose=True)
+    dX, _ = fp8.mx_gemm_fprop(A, Bt, None, fp8.EPI_NONE, want_aux=False)
+    torch.cuda.synchronize()
+    assert fp8.device_status() == 0
+    ri, ci = sample_indices(m, 40, 19), sample_indices(k, 40, 20)
+    qa, ea = oracle.mx_quantize(workloads.bits(dz[ri]), E5M2)
+    qb, eb = oracle.mx_quantize(workloads.bits(w[:, ci]), E4M3, transpose=True)
+    acc, S = oracle.mx_gemm(qa, ea, E5M2, qb, eb, E4M3)
+    got = bf16_to_f64(_sel(dX, ri, ci))
+    assert_within(got, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(got), np.abs(acc))), "dX")

@@ -144,3 +144,23 @@ def test_per_tensor_step_input_grad_vs_oracle(fp8):
     acc, S = oracle.tensor_gemm(qa, sa, E5M2, qb, sb, E4M3)
     got = bf16_to_f64(dX)
     assert_within(got, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(got), np.abs(acc))), "dX")
+
+
+def test_input_grad_full_size(fp8):
+    # dX = dZ W at the training step's sizes: 8192 x 4096, contracted over the
+    # 14336 output features (112 K blocks per tile); sampled rows and columns
+    from helpers import sample_indices
+    m, k, n = workloads.TRAIN_STEP["m"], workloads.TRAIN_STEP["k"], workloads.TRAIN_STEP["n"]
+    dz = workloads.normal_bf16((m, n), 72, "dz", std=1e-2)
+    w = workloads.normal_bf16((n, k), 72, "w", std=0.02)
+    A = fp8.quantize(dz.cuda(), E5M2)
+    Bt = fp8.quantize(w.cuda(), E4M3, transpose=True)
+    dX, _ = fp8.gemm_fprop(A, Bt, None, fp8.EPI_NONE)
+    torch.cuda.synchronize()
+    assert fp8.device_status() == 0
+    ri, ci = sample_indices(m, 40, 21), sample_indices(k, 40, 22)
+    qa, sa = oracle.quantize(workloads.bits(dz[ri]), E5M2)
+    qb, sb = oracle.quantize(workloads.bits(w[:, ci]), E4M3, transpose=True)
+    acc, S = oracle.gemm(qa, sa, E5M2, qb, sb, E4M3)
+    got = bf16_to_f64(dX[torch.from_numpy(ri).cuda()][:, torch.from_numpy(ci).cuda()])
+    assert_within(got, acc, FULL_C * S + bf16_ulp(np.maximum(np.abs(got), np.abs(acc))), "dX")
